@@ -1,0 +1,150 @@
+// common.cuh -- device helpers shared by the RMSNorm kernels (sm_103a).
+//
+// BF16 vectors are held as packed 32-bit words (two BF16 per word, element
+// 2i in the low half).  Streaming tensors are read and written with the
+// evict-first cache hint; weights and broadcast style rows go through the
+// read-only path.  All conversions round to nearest even with one PTX
+// instruction; FP32 arithmetic is IEEE (the library is built without fast
+// math).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace crmsn {
+
+// ------------------------------------------------------------ BF16 / FP8 --
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Two floats -> packed BF16 pair (lo in bits 0..15), round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two floats -> packed FP8 pair (lo in bits 0..7), round to nearest even,
+// saturating to the largest finite value.  KIND 0 = E4M3FN, 1 = E5M2.
+template <int KIND>
+__device__ __forceinline__ uint32_t pack_fp8(float lo, float hi)
+{
+    uint16_t r;
+    if constexpr (KIND == 0)
+        asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// ------------------------------------------------------------ vectors ----
+// VEC BF16 elements = VEC/2 packed words.  VEC is 8 (16-byte accesses) or 2
+// (4-byte accesses).
+
+template <int VEC>
+struct BVec {
+    uint32_t w[VEC / 2];
+};
+
+template <int VEC>
+__device__ __forceinline__ BVec<VEC> ld_stream(const uint16_t *p)
+{
+    BVec<VEC> v;
+    if constexpr (VEC == 8)
+        asm volatile("ld.global.cs.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                     : "l"(p));
+    else
+        asm volatile("ld.global.cs.u32 %0, [%1];" : "=r"(v.w[0]) : "l"(p));
+    return v;
+}
+
+template <int VEC>
+__device__ __forceinline__ BVec<VEC> ld_keep(const uint16_t *p)
+{
+    BVec<VEC> v;
+    if constexpr (VEC == 8)
+        asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                     : "l"(p));
+    else
+        asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v.w[0]) : "l"(p));
+    return v;
+}
+
+template <int VEC>
+__device__ __forceinline__ void st_stream(uint16_t *p, const BVec<VEC> &v)
+{
+    if constexpr (VEC == 8)
+        asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
+                     :: "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3])
+                     : "memory");
+    else
+        asm volatile("st.global.cs.u32 [%0], %1;" :: "l"(p), "r"(v.w[0]) : "memory");
+}
+
+// VEC FP8 codes (VEC bytes) stored from VEC/4 (VEC=8) or a half word (VEC=2).
+template <int VEC>
+__device__ __forceinline__ void st_fp8(uint8_t *p, const uint32_t (&c)[VEC / 2])
+{
+    // c[i] holds the FP8 pair of elements 2i, 2i+1 in its low 16 bits.
+    if constexpr (VEC == 8) {
+        uint32_t a = (c[0] & 0xffffu) | (c[1] << 16);
+        uint32_t b = (c[2] & 0xffffu) | (c[3] << 16);
+        asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" :: "l"(p), "r"(a), "r"(b) : "memory");
+    } else {
+        uint16_t a = (uint16_t)c[0];
+        asm volatile("st.global.cs.u16 [%0], %1;" :: "l"(p), "h"(a) : "memory");
+    }
+}
+
+// VEC FP32 weights (read-only path).
+template <int VEC>
+__device__ __forceinline__ void ld_f32_keep(const float *p, float (&f)[VEC])
+{
+    if constexpr (VEC == 8) {
+        asm volatile("ld.global.nc.v4.f32 {%0,%1,%2,%3}, [%4];"
+                     : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3]) : "l"(p));
+        asm volatile("ld.global.nc.v4.f32 {%0,%1,%2,%3}, [%4];"
+                     : "=f"(f[4]), "=f"(f[5]), "=f"(f[6]), "=f"(f[7]) : "l"(p + 4));
+    } else {
+        asm volatile("ld.global.nc.v2.f32 {%0,%1}, [%2];" : "=f"(f[0]), "=f"(f[1]) : "l"(p));
+    }
+}
+
+// ------------------------------------------------- compensated reductions --
+// A value is carried as an unevaluated pair (hi, lo); TwoSum keeps the
+// rounding error of every addition, so a tree of pair additions returns the
+// sum with an error of a few units in the last place of lo.  TwoSum is
+// symmetric in its operands, so both partners of a butterfly exchange end up
+// with identical pairs.
+
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e)
+{
+    s = __fadd_rn(a, b);
+    float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+__device__ __forceinline__ void pair_add(float &h, float &l, float bh, float bl)
+{
+    float s, e;
+    two_sum(h, bh, s, e);
+    e = __fadd_rn(e, __fadd_rn(l, bl));
+    h = __fadd_rn(s, e);
+    l = __fsub_rn(e, __fsub_rn(h, s));
+}
+
+// Butterfly over `width` lanes (power of two <= 32, aligned groups).
+__device__ __forceinline__ void pair_reduce_lanes(float &h, float &l, int width)
+{
+    for (int o = width >> 1; o > 0; o >>= 1) {
+        float bh = __shfl_xor_sync(0xffffffffu, h, o);
+        float bl = __shfl_xor_sync(0xffffffffu, l, o);
+        pair_add(h, l, bh, bl);
+    }
+}
+
+}  // namespace crmsn

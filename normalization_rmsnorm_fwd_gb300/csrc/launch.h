@@ -1,0 +1,77 @@
+// launch.h -- parameter blocks and launch entry points shared between the
+// host ABI (api.cu) and the kernel translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace crmsn {
+
+// Largest CTA of the forward kernel (its __launch_bounds__) and of the
+// backward kernel.
+constexpr int kFwdMaxThreads = 512;
+constexpr int kBwdMaxThreads = 512;
+// The backward workspace holds at most this many partial rows per SM.
+constexpr int kBwdMaxCtasPerSm = 2;
+
+enum InKind { IN_PLAIN = 0, IN_RESIDUAL = 1, IN_GATED = 2 };
+enum OutKind {
+    OUT_Y = 0,         // y = bf16(o)
+    OUT_Q = 1,         // q = fp8(o / scale)
+    OUT_BLOCK = 2,     // normed = bf16(o); 1x128 block FP8 + block scales
+    OUT_ADA = 3,       // out = bf16(o * (1 + sc) + sh); gate_out copy
+    OUT_ADA_Q = 4      // out = e4m3((o * (1 + sc) + sh) / scale); gate_out copy
+};
+
+struct FwdParams {
+    const uint16_t *x;   int64_t ldx;
+    const uint16_t *r;   int64_t ldr;     // residual stream (in)
+    const uint16_t *gate; int64_t ldgate;
+    const void *w;       float bias;      float eps;
+    int64_t T;           int H;
+    uint16_t *y;         int64_t ldy;     // y / normed / ada out
+    uint16_t *hn;        int64_t ldh;     // h_new (may equal r)
+    float *rstd;                          // nullable
+    uint8_t *q;          int64_t ldq;     // FP8 out
+    const float *scale;                   // static FP8 scale (device)
+    float *bscale;       int64_t ldT;     // block scales [H/128][ldT]
+    const uint16_t *style; int64_t lds;   // style row stride (0: broadcast)
+    uint16_t *gate_out;  int64_t ldgo;
+    int tpr;             int rpc;
+};
+
+struct BwdParams {
+    const uint16_t *g;   int64_t ldg;
+    const uint16_t *x;   int64_t ldx;
+    const void *w;       float bias;
+    const float *rstd;
+    const uint16_t *gres; int64_t ldgr;
+    uint16_t *dx;        int64_t lddx;
+    float *part;                          // [nchunk][H] partial dw rows
+    int64_t T;           int H;
+    int nchunk;          int tpr;         int rpc;
+};
+
+// Row layout picked by the host: VEC elements per access, VPT accesses per
+// thread, tpr threads per row (SUB: a power of two <= 32), rpc rows per CTA.
+struct Layout {
+    int vec, vpt, tpr, rpc;
+    bool sub;
+};
+
+// Forward launches, one per epilogue family (fwd_*.cu).
+cudaError_t launch_fwd_y(const FwdParams &p, int in, bool w32, const Layout &L, cudaStream_t s);
+cudaError_t launch_fwd_q(const FwdParams &p, int in, bool w32, int fp8k, const Layout &L, cudaStream_t s);
+cudaError_t launch_fwd_block(const FwdParams &p, const Layout &L, cudaStream_t s);
+cudaError_t launch_fwd_ada(const FwdParams &p, bool gated_fp8, const Layout &L, cudaStream_t s);
+
+// Backward (bwd.cu).
+// Picks the chunk count (resident CTAs per SM x sms, at most
+// kBwdMaxCtasPerSm x sms and at most one per row group), launches the dx /
+// partial-dw kernel and then the fixed-order dw reduction.
+cudaError_t launch_bwd(BwdParams p, bool w32, bool gres, const Layout &L, int sms, float *dw,
+                       cudaStream_t s);
+
+}  // namespace crmsn

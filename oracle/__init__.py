@@ -198,15 +198,15 @@ class Oracle:
         return out
 
     # -- operations -------------------------------------------------------------
-    def rmsnorm_fwd(self, x, w, eps, residual=None, weight_bias=0.0):
+    def rmsnorm_fwd(self, x, w, eps, residual=None, weight_bias=0.0, want_y=True):
         x, ldx = _rows(x, np.uint16)
         T, H = x.shape
         w, is32 = _weight(w)
         ldr = 0
         if residual is not None:
             residual, ldr = _rows(residual, np.uint16)
-        y_exact = np.empty((T, H), np.float64)
-        y = np.empty((T, H), np.uint16)
+        y_exact = np.empty((T, H), np.float64) if want_y else None
+        y = np.empty((T, H), np.uint16) if want_y else None
         rstd_exact = np.empty(T, np.float64)
         rstd32 = np.empty(T, np.float32)
         h_new = np.empty((T, H), np.uint16) if residual is not None else None
@@ -215,7 +215,7 @@ class Oracle:
                                _ptr(rstd_exact), _ptr(rstd32), _ptr(h_new))
         return dict(y_exact=y_exact, y=y, rstd_exact=rstd_exact, rstd=rstd32, h_new=h_new)
 
-    def rmsnorm_bwd(self, g, x, w, rstd, weight_bias=0.0, g_res=None):
+    def rmsnorm_bwd(self, g, x, w, rstd, weight_bias=0.0, g_res=None, want_dx=True):
         g, ldg = _rows(g, np.uint16)
         x, ldx = _rows(x, np.uint16)
         T, H = x.shape
@@ -224,8 +224,8 @@ class Oracle:
         ldgr = 0
         if g_res is not None:
             g_res, ldgr = _rows(g_res, np.uint16)
-        dx_exact = np.empty((T, H), np.float64)
-        dx = np.empty((T, H), np.uint16)
+        dx_exact = np.empty((T, H), np.float64) if want_dx else None
+        dx = np.empty((T, H), np.uint16) if want_dx else None
         m = np.empty(T, np.float64)
         dw = np.empty(H, np.float64)
         dw_abs = np.empty(H, np.float64)
