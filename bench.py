@@ -1,0 +1,465 @@
+#!/usr/bin/env python3
+"""Benchmark: RMSNorm forward + backward throughput on GB300.
+
+One step = the whole hot path on one batch of the headline workload
+(T=16384 rows, H=4096, BF16, fused residual route): rmsnorm_fwd (x, residual
+-> y, h_new, rstd) then rmsnorm_bwd (g, h_new, rstd -> dx, deterministic dw).
+The backward of step k reads the h_new / rstd written by the forward of step
+k-1 (two alternating buffers), so it streams from HBM as a training backward
+would instead of re-reading what the forward just left in L2; every tensor is
+128 MiB, larger than the 129 MB L2 taken together with the rest of the step.
+
+Metric: achieved HBM GB/s = algorithmic bytes of the step / step time
+(forward 536,944,640 B + backward 402,743,296 B), plus rows/s.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs an independent replica (the path
+needs no exchange); value = bytes of all ranks / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+T_ROWS, H = 16384, 4096
+FWD_BYTES = 4 * T_ROWS * H * 2 + H * 2 + T_ROWS * 4           # x, residual in; y, h_new out; w; rstd
+BWD_BYTES = 3 * T_ROWS * H * 2 + T_ROWS * 4 + H * 2 + H * 4    # g, x in; dx out; rstd; w; dw
+STEP_BYTES = FWD_BYTES + BWD_BYTES
+METRIC = "RMSNorm fwd/bwd achieved HBM GB/s (% of GB300 peak) and rows/s, H=4096 T=16K"
+WORKLOAD = ("fused residual-add RMSNorm forward + backward, T=16384, H=4096, BF16 x, residual, "
+            "g ~ N(0,1), BF16 w = 1 + 0.1 N(0,1), eps = 1e-6, deterministic FP32 dw")
+CSRC = os.path.join(ROOT, "normalization_rmsnorm_fwd_gb300", "csrc")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for d in (CSRC, os.path.join(ROOT, "include")):
+        for f in sorted(os.listdir(d)):
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> tuple[float, str]:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernels changed since it was captured."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    return d.get("kernels", {}).get(kernel, {}).get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax = float(p[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- CPU side --
+
+def oracle_sample(rows: int, seed: int = 0):
+    """Time the oracle on `rows` rows of the workload (forward + backward)."""
+    import oracle
+    from normalization_rmsnorm_fwd_gb300 import synth
+    o = oracle.default()
+    d = synth.residual_large(seed=seed, T=rows)
+    t0 = time.perf_counter()
+    f = o.rmsnorm_fwd(d["x"], d["w"], d["eps"], residual=d["residual"])
+    o.rmsnorm_bwd(d["g"], f["h_new"], d["w"], f["rstd"])
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(target_s: float = 12.0) -> dict:
+    rows, reps, spent = 256, 0, 0.0
+    while spent < target_s:
+        spent += oracle_sample(rows, seed=reps)
+        reps += 1
+    gbs = STEP_BYTES * (rows * reps / T_ROWS) / spent / 1e9
+    return {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{reps} x {rows} rows of the T=16384, H=4096 fused residual fwd+bwd "
+                      f"workload, single-threaded FP64 C oracle, {spent:.1f} s",
+            "rows_per_s": rows * reps / spent}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    rows = 256
+    for _ in range(args.warmup):
+        oracle_sample(rows)
+    times = [oracle_sample(rows, seed=i + 1) for i in range(args.steps)]
+    step_s = sum(times) / len(times)
+    gbs = STEP_BYTES * (rows / T_ROWS) / step_s / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD + f"; each step a {rows}-row sample",
+                       "T": T_ROWS, "H": H, "rows_per_step": rows},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{rows} rows per step of the T=16384, H=4096 workload"},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "rows_per_s": rows / step_s}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU side --
+
+def time_kernel(fn, iters: int, flush=None):
+    """Average device time (us) of fn() over iters launches, CUDA events on
+    the current stream; optional L2 flush between launches (not timed)."""
+    import torch
+    st = torch.cuda.current_stream()
+    total = 0.0
+    for _ in range(iters):
+        if flush is not None:
+            flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        fn()
+        b.record(st)
+        b.synchronize()
+        total += a.elapsed_time(b)
+    return total / iters * 1e3
+
+
+def other_kernels(dev, peak):
+    """Each remaining hot-path kernel at its own workload, L2 flushed before
+    every timed launch (the Ada working sets fit in L2)."""
+    import numpy as np
+    import torch
+
+    import normalization_rmsnorm_fwd_gb300 as crm
+
+    flush_buf = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    def randn(*shape):
+        return torch.randn(*shape, device=dev, dtype=torch.float32).to(torch.bfloat16)
+
+    out = []
+
+    def add(name, fn, nbytes, iters=20):
+        fn()
+        us = time_kernel(fn, iters, flush)
+        gbs = nbytes / us / 1e3
+        out.append({"kernel": name, "bytes": nbytes, "us": round(us, 2),
+                    "gbs": round(gbs, 1), "frac": round(gbs / peak, 4)})
+
+    T, Hh = 16384, 4096
+    x, r = randn(T, Hh), randn(T, Hh)
+    w = (1 + 0.1 * torch.randn(Hh, device=dev)).to(torch.bfloat16)
+    y = torch.empty_like(x)
+    rstd = torch.empty(T, device=dev)
+    add("rmsnorm_fwd plain T=16384 H=4096", lambda: crm.rmsnorm_fwd(x, w, y=y, rstd=rstd),
+        2 * T * Hh * 2 + Hh * 2 + T * 4)
+    del x, r, y
+    T5, H5 = 16384, 5120
+    x5 = (4 * torch.randn(T5, H5, device=dev)).to(torch.bfloat16)
+    w5 = 0.02 * torch.randn(H5, device=dev)
+    y5 = torch.empty_like(x5)
+    r5 = torch.empty(T5, device=dev)
+    add("rmsnorm_fwd FP32 zero-centred weight T=16384 H=5120",
+        lambda: crm.rmsnorm_fwd(x5, w5, weight_bias=1.0, y=y5, rstd=r5),
+        2 * T5 * H5 * 2 + H5 * 4 + T5 * 4)
+    del x5, y5
+    T4 = H4 = 8192
+    x4, r4 = randn(T4, H4), randn(T4, H4)
+    w4 = (1 + 0.1 * torch.randn(H4, device=dev)).to(torch.bfloat16)
+    q4 = torch.empty((T4, H4), dtype=torch.float8_e4m3fn, device=dev)
+    sc = torch.tensor([0.04], device=dev)
+    add("fused_add_rmsnorm_quant e4m3 T=H=8192",
+        lambda: crm.fused_add_rmsnorm_quant(q4, x4, r4, w4, sc), 469_778_436)
+    nb = torch.empty((H4 // 128, T4), device=dev)
+    n4 = torch.empty_like(x4)
+    add("fused_add_rmsnorm_fp8_block_quant T=H=8192",
+        lambda: crm.fused_add_rmsnorm_fp8_block_quant(q4, nb, n4, x4, r4, w4), 606_093_312)
+    del x4, r4, q4, n4
+    T6, D = 2520, 3072
+    x6, u6, g6 = randn(T6, D), randn(T6, D), randn(T6, D)
+    st, st1 = randn(T6, 3 * D), randn(1, 3 * D)
+    w6 = torch.ones(D, dtype=torch.bfloat16, device=dev)
+    o6, go6 = torch.empty_like(x6), torch.empty_like(x6)
+    q6 = torch.empty((T6, D), dtype=torch.float8_e4m3fn, device=dev)
+    add("ada_rms_norm_style per-row style T=2520 D=3072",
+        lambda: crm.ada_rms_norm_style(x6, w6, st, out=o6, gate_out=go6), 92_903_424)
+    add("ada_rms_norm_style broadcast style T=2520 D=3072",
+        lambda: crm.ada_rms_norm_style(x6, w6, st1, out=o6, gate_out=go6), 46_473_216)
+    add("gate_residual_ada_norm_fp8 per-row style T=2520 D=3072",
+        lambda: crm.gate_residual_ada_norm_fp8(u6, x6, g6, w6, st, sc, out=q6, gate_out=go6),
+        131_610_628)
+    add("gate_residual_ada_norm_fp8 broadcast style T=2520 D=3072",
+        lambda: crm.gate_residual_ada_norm_fp8(u6, x6, g6, w6, st1, sc, out=q6, gate_out=go6),
+        85_180_420)
+    del flush_buf
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args):
+    import torch
+
+    import normalization_rmsnorm_fwd_gb300 as crm
+    from normalization_rmsnorm_fwd_gb300 import _abi, synth
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    torch.manual_seed(rank)
+    _abi.load()
+    peak, peak_kind = measured_peaks()
+
+    # Inputs: the seeded host generator, copied once into HBM.
+    d = synth.residual_large(seed=rank)
+
+    def to_dev(bits):
+        return torch.from_numpy(bits.view("int16")).view(torch.bfloat16).to(dev)
+
+    x, r, g, w = to_dev(d["x"]), to_dev(d["residual"]), to_dev(d["g"]), to_dev(d["w"])
+    y = torch.empty_like(x)
+    dx = torch.empty_like(x)
+    hn = [torch.empty_like(x), torch.empty_like(x)]
+    rs = [torch.empty(T_ROWS, device=dev), torch.empty(T_ROWS, device=dev)]
+    dw = torch.empty(H, device=dev)
+    ws = crm.rmsnorm_bwd_workspace(T_ROWS, H, dev)
+    crm.rmsnorm_fwd(x, w, 1e-6, residual=r, y=y, rstd=rs[1], h_new=hn[1])   # step -1's output
+
+    st = torch.cuda.current_stream(dev)
+
+    def step(k, ev=None):
+        a, b = k % 2, (k + 1) % 2
+        if ev is not None:
+            ev[0].record(st)
+        crm.rmsnorm_fwd(x, w, 1e-6, residual=r, y=y, rstd=rs[a], h_new=hn[a])
+        if ev is not None:
+            ev[1].record(st)
+        crm.rmsnorm_bwd(g, hn[b], w, rs[b], dx=dx, dw=dw, workspace=ws)
+        if ev is not None:
+            ev[2].record(st)
+
+    for k in range(args.warmup):
+        step(k)
+    torch.cuda.synchronize()
+
+    # Timed region: exactly K steps, barrier + synchronize on both sides.
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(st)
+    for k in range(args.steps):
+        step(k)
+    t_end.record(st)
+    torch.cuda.synchronize()
+    barrier(world)
+    clock = clocks.stop()
+    ms_total = t_start.elapsed_time(t_end)
+    ms_total = max_over_ranks(ms_total, world, dev)
+    ms_step = ms_total / args.steps
+
+    # Per-kernel durations (same stream, events between the two calls).
+    nsplit = max(args.steps, 20)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(nsplit)]
+    for k in range(nsplit):
+        step(k, evs[k])
+    torch.cuda.synchronize()
+    fwd_us = sum(e[0].elapsed_time(e[1]) for e in evs) / nsplit * 1e3
+    bwd_us = sum(e[1].elapsed_time(e[2]) for e in evs) / nsplit * 1e3
+
+    # End to end through the public API with host buffers: pinned inputs
+    # copied in, both calls, every output copied back, all inside the timing.
+    e2e = None
+    if rank == 0 or world > 1:
+        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+        hx, hr, hg = pin(x), pin(r), pin(g)
+        hx.copy_(x); hr.copy_(r); hg.copy_(g)
+        oy, ohn, odx, ors, odw = pin(y), pin(y), pin(y), pin(rs[0]), pin(dw)
+        h2d = 3 * T_ROWS * H * 2
+        d2h = 3 * T_ROWS * H * 2 + T_ROWS * 4 + H * 4
+
+        def e2e_step():
+            x.copy_(hx, non_blocking=True)
+            r.copy_(hr, non_blocking=True)
+            g.copy_(hg, non_blocking=True)
+            crm.rmsnorm_fwd(x, w, 1e-6, residual=r, y=y, rstd=rs[0], h_new=hn[0])
+            crm.rmsnorm_bwd(g, hn[0], w, rs[0], dx=dx, dw=dw, workspace=ws)
+            oy.copy_(y, non_blocking=True)
+            ohn.copy_(hn[0], non_blocking=True)
+            odx.copy_(dx, non_blocking=True)
+            ors.copy_(rs[0], non_blocking=True)
+            odw.copy_(dw, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        ne = max(3, min(args.steps, 20))
+        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        a_ev.record(st)
+        for _ in range(ne):
+            e2e_step()
+        b_ev.record(st)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(a_ev.elapsed_time(b_ev) / ne, world, dev)
+        e2e = {"value": world * STEP_BYTES / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e2e_ms}
+        del hx, hr, hg, oy, ohn, odx, ors, odw
+
+    per_kernel = None
+    if rank == 0 and not args.no_extra:
+        del x, r, g, y, dx, hn, rs
+        torch.cuda.empty_cache()
+        per_kernel = other_kernels(dev, peak)
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    fwd_gbs = FWD_BYTES / fwd_us / 1e3
+    bwd_gbs = BWD_BYTES / bwd_us / 1e3
+    value = world * STEP_BYTES / (ms_step * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "T": T_ROWS, "H": H, "io_dtype": "bf16",
+                   "global_batch_rows": world * T_ROWS, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: 128 MiB tensors, and the backward reads the "
+                         "h_new written one step earlier"},
+        "rows_per_s": round(world * T_ROWS / (ms_step * 1e-3)),
+        "pct_of_peak": {"measured_copy_gbs": peak, "frac_measured": round(value / world / peak, 4),
+                        "nominal_gbs": 8000.0, "frac_nominal": round(value / world / 8000.0, 4)},
+        "roofline": {"bound": "hbm", "kernel": "rmsnorm_fwd fused residual (dominant)",
+                     "achieved": round(fwd_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(fwd_gbs / peak, 4), "peak_kind": peak_kind + " hbm_gbs",
+                     "bytes_per_launch": FWD_BYTES, "us_per_launch": round(fwd_us, 2),
+                     "traffic": ncu_traffic("rmsnorm_fwd")},
+        "backward": {"achieved": round(bwd_gbs, 1), "frac": round(bwd_gbs / peak, 4),
+                     "bytes_per_call": BWD_BYTES, "us_per_call": round(bwd_us, 2),
+                     "launches_per_call": 2, "traffic": ncu_traffic("rmsnorm_bwd")},
+        "clocks": clock,
+        "e2e": e2e,
+        "gpu_launches": 3 * args.steps,
+        "per_kernel": per_kernel,
+    }
+    if not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline()
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-extra", action="store_true", help="skip the per-kernel table")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -30,7 +30,8 @@
  *   - Arithmetic: BF16 inputs, FP32 statistics with IEEE square root and
  *     division (no fast math), one rounding to the output format.
  *   - Every argument is checked before anything is enqueued; on an error
- *     nothing is launched.  T == 0 returns CRMSN_OK without a launch.
+ *     nothing is launched.  T == 0 returns CRMSN_OK without a launch (row
+ *     pointers may then be NULL; rmsnorm_bwd still zeroes dw).
  *   - In-place use: an output may be the very same tensor (same pointer and
  *     stride) as the input it replaces, as listed per function.  Any other
  *     overlap between an output and another tensor returns CRMSN_ERR_ALIAS.

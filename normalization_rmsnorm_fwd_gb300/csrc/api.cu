@@ -277,10 +277,10 @@ crmsn_status rmsnorm_fwd(const void *x, int64_t ldx, const void *residual, int64
     if (T < 0) return CRMSN_ERR_SHAPE;
     if (crmsn_status s = check_h(H)) return s;
     if (w_dtype != CRMSN_BF16 && w_dtype != CRMSN_F32) return CRMSN_ERR_DTYPE;
-    if (!x || !w || !y || (residual && !h_new)) return CRMSN_ERR_NULL;
     if (bad_float(eps) || eps < 0.f || bad_float(weight_bias)) return CRMSN_ERR_ARG;
-    if (T > 1 && (ldx < H || ldy < H || (residual && (ldr < H || ldh < H)))) return CRMSN_ERR_SHAPE;
     if (T == 0) return CRMSN_OK;
+    if (!x || !w || !y || (residual && !h_new)) return CRMSN_ERR_NULL;
+    if (T > 1 && (ldx < H || ldy < H || (residual && (ldr < H || ldh < H)))) return CRMSN_ERR_SHAPE;
     const int wes = w_dtype == CRMSN_F32 ? 4 : 2;
     const bool res = residual != nullptr;
     const Tensor ts[] = {
@@ -330,8 +330,13 @@ crmsn_status rmsnorm_bwd(const void *g, int64_t ldg, const void *x, int64_t ldx,
     if (T < 0) return CRMSN_ERR_SHAPE;
     if (crmsn_status s = check_h(H)) return s;
     if (w_dtype != CRMSN_BF16 && w_dtype != CRMSN_F32) return CRMSN_ERR_DTYPE;
-    if (!g || !x || !w || !rstd || !dx || !dw || !workspace) return CRMSN_ERR_NULL;
     if (bad_float(weight_bias)) return CRMSN_ERR_ARG;
+    if (!dw) return CRMSN_ERR_NULL;
+    if (T == 0) {
+        if (!al(dw, 4)) return CRMSN_ERR_ALIGNMENT;
+        return launched(cudaMemsetAsync(dw, 0, (size_t)H * sizeof(float), stream));
+    }
+    if (!g || !x || !w || !rstd || !dx || !workspace) return CRMSN_ERR_NULL;
     if (T > 1 && (ldg < H || ldx < H || lddx < H || (g_residual && ldgr < H))) return CRMSN_ERR_SHAPE;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return launched(cudaErrorNoDevice);
@@ -349,11 +354,8 @@ crmsn_status rmsnorm_bwd(const void *g, int64_t ldg, const void *x, int64_t ldx,
         {{dw, 1, H, H, 4}, true, -1},
         {{workspace, 1, (int64_t)workspace_bytes, (int64_t)workspace_bytes, 1}, true, -1},
     };
-    if (T > 0)
-        if (crmsn_status s = check_alias(ts, 8)) return s;
+    if (crmsn_status s = check_alias(ts, 8)) return s;
     if (!al(dw, 4) || !al(rstd, 4)) return CRMSN_ERR_ALIGNMENT;
-    if (T == 0)
-        return launched(cudaMemsetAsync(dw, 0, (size_t)H * sizeof(float), stream));
     const Access acc[] = {{g, ldg, 0}, {x, ldx, 0}, {dx, lddx, 0}, {g_residual, ldgr, 0},
                           {w, 0, w_dtype == CRMSN_F32 ? 3 : 2}};
     const int vec = pick_vec(acc, 5, H, T);
@@ -382,10 +384,10 @@ crmsn_status fused_add_rmsnorm_quant(void *out, int64_t ldo, int fp8_kind, const
     if (crmsn_status s = check_h(H)) return s;
     if (w_dtype != CRMSN_BF16 && w_dtype != CRMSN_F32) return CRMSN_ERR_DTYPE;
     if (fp8_kind != CRMSN_E4M3 && fp8_kind != CRMSN_E5M2) return CRMSN_ERR_DTYPE;
-    if (!out || !x || !w || !scale) return CRMSN_ERR_NULL;
     if (bad_float(eps) || eps < 0.f || bad_float(weight_bias)) return CRMSN_ERR_ARG;
-    if (T > 1 && (ldo < H || ldx < H || (residual && ldr < H))) return CRMSN_ERR_SHAPE;
     if (T == 0) return CRMSN_OK;
+    if (!out || !x || !w || !scale) return CRMSN_ERR_NULL;
+    if (T > 1 && (ldo < H || ldx < H || (residual && ldr < H))) return CRMSN_ERR_SHAPE;
     const int wes = w_dtype == CRMSN_F32 ? 4 : 2;
     const Tensor ts[] = {
         {{x, T, ldx, H, 2}, false, -1},
@@ -425,10 +427,11 @@ crmsn_status fused_add_rmsnorm_fp8_block_quant(void *out, float *block_scale, in
 {
     if (T < 0 || H < 1) return CRMSN_ERR_SHAPE;
     if (H % 128 || H > CRMSN_MAX_H) return CRMSN_ERR_UNSUPPORTED_H;
-    if (!out || !block_scale || !normed_out || !x || !residual || !w) return CRMSN_ERR_NULL;
     if (bad_float(eps) || eps < 0.f) return CRMSN_ERR_ARG;
-    if (ldT < T || (T > 1 && (ldx < H || ldr < H))) return CRMSN_ERR_SHAPE;
+    if (ldT < T) return CRMSN_ERR_SHAPE;
     if (T == 0) return CRMSN_OK;
+    if (!out || !block_scale || !normed_out || !x || !residual || !w) return CRMSN_ERR_NULL;
+    if (T > 1 && (ldx < H || ldr < H)) return CRMSN_ERR_SHAPE;
     const Tensor ts[] = {
         {{x, T, ldx, H, 2}, false, -1},
         {{w, 1, H, H, 2}, false, -1},
@@ -464,10 +467,10 @@ static crmsn_status ada_common(void *residual, const void *x, const void *gate, 
 {
     if (T < 0 || D < 1 || (D & 1)) return CRMSN_ERR_SHAPE;
     if (D > CRMSN_MAX_H) return CRMSN_ERR_UNSUPPORTED_H;
-    if (!x || !w || !style || !out || !gate_out) return CRMSN_ERR_NULL;
-    if (gated && (!residual || !gate || !scale)) return CRMSN_ERR_NULL;
     if (bad_float(eps) || eps < 0.f) return CRMSN_ERR_ARG;
     if (T == 0) return CRMSN_OK;
+    if (!x || !w || !style || !out || !gate_out) return CRMSN_ERR_NULL;
+    if (gated && (!residual || !gate || !scale)) return CRMSN_ERR_NULL;
     if (style_rows != 1 && style_rows != T) return CRMSN_ERR_SHAPE;
     const int oes = gated ? 1 : 2;
     const Tensor ts[] = {

@@ -74,6 +74,7 @@ def test_fwd_validation(L):
     assert fwd(L, eps=-1.0) == ARG
     assert fwd(L, ldx=100) == SHAPE
     assert fwd(L, T=0) == OK                                        # no launch, no CUDA call
+    assert fwd(L, T=0, x=None, y=None) == OK                        # empty tensors: NULL data
     assert fwd(L, x=A + 1) == ALIGN                                 # not even 4-byte aligned
     assert fwd(L, ldx=257) == ALIGN                                 # odd row stride
 
