@@ -1,0 +1,374 @@
+// bwd.cuh -- RMSNorm backward: dx per row and a deterministic FP32 dw.
+//
+// Source: "FlashInfer normalization operator guide" 6.1-6.3 and the
+// "cake_rmsnorm_det_train_forward" Notes:
+//   m    = mean(g * w * x)
+//   dx   = bf16(rstd*g*w - x*rstd^3*m (+ g_residual))
+//   dw   = sum_t g * x * rstd, bitwise reproducible for a given T and SM count.
+//
+// Design (GB300).  CTA c owns the contiguous row chunk [c*T/n, (c+1)*T/n) of
+// a fixed chunk table (n = chunks, a function of T and the SM count).  Each
+// thread owns the same columns in every row and keeps a compensated (TwoSum)
+// FP32 dw accumulator per column in registers while it walks its chunk.
+// Rows stream through a ring of shared-memory stages filled with cp.async:
+// every thread copies exactly the 16-byte (or 4-byte) pieces of g, x
+// (g_residual) and rstd that it will itself consume, D rows ahead, and waits
+// only on its own copy groups (cp.async.wait_group), so D rows per CTA are in
+// flight without any register cost and without any cross-thread handoff or
+// flag spinning.  At the end the CTA adds its row groups in group order and
+// writes one FP32 partial row; a second kernel (bwd_reduce.cu) adds the
+// partial rows of each column in chunk order.
+#pragma once
+
+#include "launch.h"
+
+namespace crmsn {
+
+// Per-thread asynchronous global -> shared copies.
+__device__ __forceinline__ void cp_async_16(void *smem, const void *gmem)
+{
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(s), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_4(void *smem, const void *gmem)
+{
+    const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(s), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+
+// Bytes of one ring stage: NT tensors x VPT vectors per thread, plus one
+// private rstd slot per thread.
+__host__ __device__ constexpr int bwd_stage_bytes(int nt, int vpt, int vec, int threads)
+{
+    return nt * vpt * threads * vec * 2 + threads * 4;
+}
+
+template <bool W32, bool GRES, int VEC, int VPT, bool SUB, int D>
+__global__ void __launch_bounds__(kBwdMaxThreads, 1)
+k_rmsnorm_bwd(const BwdParams p)
+{
+    constexpr int NW = VEC / 2;
+    constexpr int NT = GRES ? 3 : 2;
+    constexpr int S = D + 1;                  // ring stages
+    constexpr int VB = VEC * 2;               // bytes per vector
+    __shared__ float red_h[32], red_l[32];
+    extern __shared__ __align__(16) unsigned char dyn_smem[];
+
+    const int nthr = blockDim.x;
+    const int tpr = p.tpr;
+    const int rpc = p.rpc;
+    const int grp = threadIdx.x / tpr;
+    const int lane = threadIdx.x - grp * tpr;
+    const int nvec = p.H / VEC;
+    const int64_t r0 = (int64_t)blockIdx.x * p.T / p.nchunk;
+    const int64_t r1 = (int64_t)(blockIdx.x + 1) * p.T / p.nchunk;
+    const int64_t iters = (r1 - r0 + rpc - 1) / rpc;
+
+    // Shared memory: ring [S][stage], then w_eff [H], then the row-group
+    // combine area [rpc-1][H][2].
+    const int stage_bytes = bwd_stage_bytes(NT, VPT, VEC, nthr);
+    unsigned char *ring = dyn_smem;
+    float *wsm = reinterpret_cast<float *>(dyn_smem + (size_t)S * stage_bytes);
+    float *comb = wsm + p.H;
+
+    auto slot = [&](int stage, int tensor, int k) -> unsigned char * {
+        return ring + (size_t)stage * stage_bytes + ((size_t)(tensor * VPT + k) * nthr + threadIdx.x) * VB;
+    };
+    auto rslot = [&](int stage) -> float * {
+        return reinterpret_cast<float *>(ring + (size_t)stage * stage_bytes +
+                                         (size_t)NT * VPT * nthr * VB) + threadIdx.x;
+    };
+    // Issue the copies of iteration `it` (row r0 + grp + it*rpc) into its stage.
+    auto issue = [&](int64_t it) {
+        const int64_t t = r0 + grp + it * rpc;
+        if (it < iters && t < r1) {
+            const int stage = (int)(it % S);
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int v = k * tpr + lane;
+                if (v < nvec) {
+                    const int64_t c = (int64_t)v * VEC;
+                    if constexpr (VEC == 8) {
+                        cp_async_16(slot(stage, 0, k), p.g + t * p.ldg + c);
+                        cp_async_16(slot(stage, 1, k), p.x + t * p.ldx + c);
+                        if constexpr (GRES) cp_async_16(slot(stage, 2, k), p.gres + t * p.ldgr + c);
+                    } else {
+                        cp_async_4(slot(stage, 0, k), p.g + t * p.ldg + c);
+                        cp_async_4(slot(stage, 1, k), p.x + t * p.ldx + c);
+                        if constexpr (GRES) cp_async_4(slot(stage, 2, k), p.gres + t * p.ldgr + c);
+                    }
+                }
+            }
+            cp_async_4(rslot(stage), p.rstd + t);
+        }
+        cp_async_commit();   // one group per iteration, empty or not
+    };
+
+    // Prologue: the first D rows go in flight while the weight is prepared.
+#pragma unroll
+    for (int i = 0; i < D; ++i) issue(i);
+
+    // Effective weight f32(w + bias) of this thread's columns, in shared
+    // memory; group 0 writes it, the other groups read it after a barrier.
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = k * tpr + lane;
+        if (grp == 0 && v < nvec) {
+            const int64_t c = (int64_t)v * VEC;
+            if constexpr (W32) {
+                float f[VEC];
+                ld_f32_keep<VEC>(static_cast<const float *>(p.w) + c, f);
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) wsm[c + i] = __fadd_rn(f[i], p.bias);
+            } else {
+                BVec<VEC> wb = ld_keep<VEC>(static_cast<const uint16_t *>(p.w) + c);
+#pragma unroll
+                for (int i = 0; i < NW; ++i) {
+                    wsm[c + 2 * i] = __fadd_rn(bf_lo(wb.w[i]), p.bias);
+                    wsm[c + 2 * i + 1] = __fadd_rn(bf_hi(wb.w[i]), p.bias);
+                }
+            }
+        }
+    }
+    if (rpc > 1) __syncthreads();
+
+    float acc[VPT][VEC], cmp[VPT][VEC];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) { acc[k][i] = 0.f; cmp[k][i] = 0.f; }
+
+    for (int64_t it = 0; it < iters; ++it) {
+        const int64_t t = r0 + grp + it * rpc;
+        const bool live = t < r1;
+        const int stage = (int)(it % S);
+        issue(it + D);                       // keep D rows ahead in flight
+        cp_async_wait<D>();                  // this thread's copies of row `it` landed
+
+        BVec<VEC> gc[VPT], xc[VPT], rc[VPT];
+        float we[VPT][VEC];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = k * tpr + lane;
+            const bool ok = live && v < nvec;
+#pragma unroll
+            for (int i = 0; i < NW; ++i) {
+                gc[k].w[i] = ok ? reinterpret_cast<const uint32_t *>(slot(stage, 0, k))[i] : 0u;
+                xc[k].w[i] = ok ? reinterpret_cast<const uint32_t *>(slot(stage, 1, k))[i] : 0u;
+                if constexpr (GRES)
+                    rc[k].w[i] = ok ? reinterpret_cast<const uint32_t *>(slot(stage, 2, k))[i] : 0u;
+            }
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) we[k][i] = (v < nvec) ? wsm[v * VEC + i] : 0.f;
+        }
+        const float rs = live ? *rslot(stage) : 0.f;
+
+        // m = mean(g * w * x): FP32 per thread, compensated across threads.
+        float dot = 0.f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+#pragma unroll
+            for (int i = 0; i < NW; ++i) {
+                dot = __fmaf_rn(__fmul_rn(bf_lo(gc[k].w[i]), we[k][2 * i]), bf_lo(xc[k].w[i]), dot);
+                dot = __fmaf_rn(__fmul_rn(bf_hi(gc[k].w[i]), we[k][2 * i + 1]), bf_hi(xc[k].w[i]), dot);
+            }
+        float dh = dot, dl = 0.f;
+        if constexpr (SUB) {
+            pair_reduce_lanes(dh, dl, tpr);
+        } else {
+            pair_reduce_lanes(dh, dl, 32);
+            const int nwarp = tpr >> 5;
+            const int warp = threadIdx.x >> 5;
+            if ((threadIdx.x & 31) == 0) { red_h[warp] = dh; red_l[warp] = dl; }
+            __syncthreads();
+            const int w0 = grp * nwarp;
+            dh = red_h[w0];
+            dl = red_l[w0];
+            for (int i = 1; i < nwarp; ++i) pair_add(dh, dl, red_h[w0 + i], red_l[w0 + i]);
+            __syncthreads();   // red_* is rewritten by the next row
+        }
+        const float m = __fdiv_rn(__fadd_rn(dh, dl), (float)p.H);
+        const float c3 = __fmul_rn(__fmul_rn(__fmul_rn(rs, rs), rs), m);
+
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = k * tpr + lane;
+            float d[VEC];
+#pragma unroll
+            for (int i = 0; i < NW; ++i) {
+                const float g0 = bf_lo(gc[k].w[i]), g1 = bf_hi(gc[k].w[i]);
+                const float x0 = bf_lo(xc[k].w[i]), x1 = bf_hi(xc[k].w[i]);
+                d[2 * i] = __fmaf_rn(-x0, c3, __fmul_rn(rs, __fmul_rn(g0, we[k][2 * i])));
+                d[2 * i + 1] = __fmaf_rn(-x1, c3, __fmul_rn(rs, __fmul_rn(g1, we[k][2 * i + 1])));
+                if constexpr (GRES) {
+                    d[2 * i] = __fadd_rn(d[2 * i], bf_lo(rc[k].w[i]));
+                    d[2 * i + 1] = __fadd_rn(d[2 * i + 1], bf_hi(rc[k].w[i]));
+                }
+                // dw term g*x*rstd: g*x is exact in FP32; TwoSum keeps the
+                // accumulation error in cmp.
+                const float e0 = __fmul_rn(__fmul_rn(g0, x0), rs);
+                const float e1 = __fmul_rn(__fmul_rn(g1, x1), rs);
+                float s, err;
+                two_sum(acc[k][2 * i], e0, s, err);
+                acc[k][2 * i] = s;
+                cmp[k][2 * i] = __fadd_rn(cmp[k][2 * i], err);
+                two_sum(acc[k][2 * i + 1], e1, s, err);
+                acc[k][2 * i + 1] = s;
+                cmp[k][2 * i + 1] = __fadd_rn(cmp[k][2 * i + 1], err);
+            }
+            if (live && v < nvec) {
+                BVec<VEC> o;
+#pragma unroll
+                for (int i = 0; i < NW; ++i) o.w[i] = pack_bf16(d[2 * i], d[2 * i + 1]);
+                st_stream<VEC>(p.dx + t * p.lddx + (int64_t)v * VEC, o);
+            }
+        }
+    }
+    cp_async_wait<0>();
+
+    // Combine the CTA's row groups in group order, then write the partial row.
+    if (rpc > 1) {
+        if (grp > 0) {
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int v = k * tpr + lane;
+                if (v < nvec)
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) {
+                        float *c2 = comb + ((int64_t)(grp - 1) * p.H + (int64_t)v * VEC + i) * 2;
+                        c2[0] = acc[k][i];
+                        c2[1] = cmp[k][i];
+                    }
+            }
+        }
+        __syncthreads();
+        if (grp == 0) {
+            for (int gi = 1; gi < rpc; ++gi)
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    const int v = k * tpr + lane;
+                    if (v < nvec)
+#pragma unroll
+                        for (int i = 0; i < VEC; ++i) {
+                            const float *c2 = comb + ((int64_t)(gi - 1) * p.H + (int64_t)v * VEC + i) * 2;
+                            pair_add(acc[k][i], cmp[k][i], c2[0], c2[1]);
+                        }
+                }
+        }
+    }
+    if (grp == 0) {
+        float *prow = p.part + (int64_t)blockIdx.x * p.H;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = k * tpr + lane;
+            if (v < nvec)
+#pragma unroll
+                for (int i = 0; i < VEC; ++i)
+                    prow[(int64_t)v * VEC + i] = __fadd_rn(acc[k][i], cmp[k][i]);
+        }
+    }
+    // Let the dependent reduce grid get scheduled; it still waits for this
+    // whole grid (and its memory) with griddepcontrol.wait.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Dynamic shared memory of one CTA for a layout and prefetch depth D.
+inline size_t bwd_smem_bytes(bool gres, int vec, int vpt, int threads, int rpc, int H, int D)
+{
+    return (size_t)(D + 1) * bwd_stage_bytes(gres ? 3 : 2, vpt, vec, threads) +
+           ((size_t)H + (size_t)(rpc - 1) * H * 2) * sizeof(float);
+}
+
+// Launch of one instantiation: picks the chunk count from the occupancy of
+// this kernel (at most kBwdMaxCtasPerSm CTAs per SM, at most one chunk per
+// row group), launches it and returns the chunk count used.
+template <bool W32, bool GRES, int VEC, int VPT, bool SUB, int D>
+cudaError_t launch_bwd_inst(BwdParams p, int sms, int *nchunk_out, cudaStream_t s)
+{
+    const int threads = p.tpr * p.rpc;
+    const size_t smem = bwd_smem_bytes(GRES, VEC, VPT, threads, p.rpc, p.H, D);
+    auto kern = k_rmsnorm_bwd<W32, GRES, VEC, VPT, SUB, D>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    if (per_sm > kBwdMaxCtasPerSm) per_sm = kBwdMaxCtasPerSm;
+    const int64_t by_rows = (p.T + p.rpc - 1) / p.rpc;
+    const int64_t cap = (int64_t)per_sm * sms;
+    p.nchunk = (int)(by_rows < cap ? by_rows : cap);
+    kern<<<p.nchunk, threads, smem, s>>>(p);
+    *nchunk_out = p.nchunk;
+    return cudaGetLastError();
+}
+
+// Dispatch over layouts (SUB groups with VPT 1|2; multi-warp groups with VPT
+// 1|2|4 for 16-byte vectors, 1|2|4|8|16 for 4-byte vectors) and the prefetch
+// depth (3 rows ahead when four stages fit in shared memory, else 1).
+template <bool W32, bool GRES, int VEC, int D>
+cudaError_t launch_bwd_vd(const BwdParams &p, const Layout &L, int sms, int *nc, cudaStream_t s)
+{
+    if constexpr (D == 0) {
+        // Only the widest rows (32 elements per thread) need the unpipelined form.
+        if (!L.sub && L.vpt == 32 / VEC) return launch_bwd_inst<W32, GRES, VEC, 32 / VEC, false, 0>(p, sms, nc, s);
+        return cudaErrorInvalidConfiguration;
+    }
+    if (L.sub) {
+        if (L.vpt == 1) return launch_bwd_inst<W32, GRES, VEC, 1, true, D>(p, sms, nc, s);
+        if (L.vpt == 2) return launch_bwd_inst<W32, GRES, VEC, 2, true, D>(p, sms, nc, s);
+    } else {
+        if (L.vpt == 1) return launch_bwd_inst<W32, GRES, VEC, 1, false, D>(p, sms, nc, s);
+        if (L.vpt == 2) return launch_bwd_inst<W32, GRES, VEC, 2, false, D>(p, sms, nc, s);
+        if (L.vpt == 4) return launch_bwd_inst<W32, GRES, VEC, 4, false, D>(p, sms, nc, s);
+        if constexpr (VEC == 2) {
+            if (L.vpt == 8) return launch_bwd_inst<W32, GRES, VEC, 8, false, D>(p, sms, nc, s);
+            if (L.vpt == 16) return launch_bwd_inst<W32, GRES, VEC, 16, false, D>(p, sms, nc, s);
+        }
+    }
+    return cudaErrorInvalidConfiguration;
+}
+
+// Dynamic shared memory a backward CTA may use (the SM has 228 KB).
+constexpr size_t kBwdSmemBudget = 200 * 1024;
+
+// Prefetch depth: 3 rows ahead when four stages fit the shared-memory
+// budget, else 1, else none (only rows of 32 elements per thread at H close
+// to the maximum).
+template <bool W32>
+cudaError_t launch_bwd_weight(const BwdParams &p, bool gres, const Layout &L, int sms, int *nc,
+                              cudaStream_t s)
+{
+    const int threads = p.tpr * p.rpc;
+    auto fits = [&](int d) {
+        return bwd_smem_bytes(gres, L.vec, L.vpt, threads, p.rpc, p.H, d) <= kBwdSmemBudget;
+    };
+    const int D = fits(3) ? 3 : (fits(1) ? 1 : 0);
+    if (L.vec == 8) {
+        if (gres) return D == 3 ? launch_bwd_vd<W32, true, 8, 3>(p, L, sms, nc, s)
+                       : D == 1 ? launch_bwd_vd<W32, true, 8, 1>(p, L, sms, nc, s)
+                                : launch_bwd_vd<W32, true, 8, 0>(p, L, sms, nc, s);
+        return D == 3 ? launch_bwd_vd<W32, false, 8, 3>(p, L, sms, nc, s)
+             : D == 1 ? launch_bwd_vd<W32, false, 8, 1>(p, L, sms, nc, s)
+                      : launch_bwd_vd<W32, false, 8, 0>(p, L, sms, nc, s);
+    }
+    if (L.vec == 2) {
+        if (gres) return D == 3 ? launch_bwd_vd<W32, true, 2, 3>(p, L, sms, nc, s)
+                       : D == 1 ? launch_bwd_vd<W32, true, 2, 1>(p, L, sms, nc, s)
+                                : launch_bwd_vd<W32, true, 2, 0>(p, L, sms, nc, s);
+        return D == 3 ? launch_bwd_vd<W32, false, 2, 3>(p, L, sms, nc, s)
+             : D == 1 ? launch_bwd_vd<W32, false, 2, 1>(p, L, sms, nc, s)
+                      : launch_bwd_vd<W32, false, 2, 0>(p, L, sms, nc, s);
+    }
+    return cudaErrorInvalidConfiguration;
+}
+
+}  // namespace crmsn

@@ -70,8 +70,14 @@ cudaError_t launch_fwd_ada(const FwdParams &p, bool gated_fp8, const Layout &L, 
 // Backward (bwd.cu).
 // Picks the chunk count (resident CTAs per SM x sms, at most
 // kBwdMaxCtasPerSm x sms and at most one per row group), launches the dx /
-// partial-dw kernel and then the fixed-order dw reduction.
+// partial-dw kernel and then the fixed-order dw reduction (bwd_reduce.cu).
 cudaError_t launch_bwd(BwdParams p, bool w32, bool gres, const Layout &L, int sms, float *dw,
                        cudaStream_t s);
+// The dx / partial-dw kernel alone, per weight type (bwd_bf16w.cu,
+// bwd_f32w.cu); *nchunk receives the chunk count it used.
+cudaError_t launch_bwd_bf16w(const BwdParams &p, bool gres, const Layout &L, int sms, int *nchunk,
+                             cudaStream_t s);
+cudaError_t launch_bwd_f32w(const BwdParams &p, bool gres, const Layout &L, int sms, int *nchunk,
+                            cudaStream_t s);
 
 }  // namespace crmsn
