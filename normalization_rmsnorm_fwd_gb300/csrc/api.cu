@@ -87,9 +87,10 @@ Layout choose_fwd(int H, int vec, bool need16, bool ada)
     return L;
 }
 
-// Backward: as few vectors per thread as fit the row in kBwdMaxThreads
-// threads (one 16-byte vector per thread up to H = 4096); the software
-// prefetch keeps the next row in flight.
+// Backward: groups of at most 8 warps while a thread holds at most 16
+// elements (2 16-byte vectors), so that a row's cross-thread reduction stays
+// short and two CTAs fit per SM; wider rows grow to 16 warps, then to more
+// vectors per thread.  The cp.async ring keeps the next rows in flight.
 Layout choose_bwd(int H, int vec)
 {
     const int nvec = H / vec;
@@ -104,10 +105,12 @@ Layout choose_bwd(int H, int vec)
         L.rpc = 256 / tpr;
         return L;
     }
+    auto nw = [&](int vpt) { return (nvec + 32 * vpt - 1) / (32 * vpt); };
     int vpt = 1;
-    while ((nvec + 32 * vpt - 1) / (32 * vpt) > kBwdMaxThreads / 32) vpt *= 2;
+    while (nw(vpt) > 8 && vpt * vec < 16) vpt *= 2;
+    while (nw(vpt) > kBwdMaxThreads / 32) vpt *= 2;
     L.vpt = vpt;
-    L.tpr = 32 * ((nvec + 32 * vpt - 1) / (32 * vpt));
+    L.tpr = 32 * nw(vpt);
     L.sub = false;
     L.rpc = L.tpr >= 256 ? 1 : 256 / L.tpr;
     return L;

@@ -8,8 +8,10 @@
 //
 // Design (GB300).  CTA c owns the contiguous row chunk [c*T/n, (c+1)*T/n) of
 // a fixed chunk table (n = chunks, a function of T and the SM count).  Each
-// thread owns the same columns in every row and keeps a compensated (TwoSum)
-// FP32 dw accumulator per column in registers while it walks its chunk.
+// thread owns the same columns in every row and keeps, per column, a plain
+// FP32 sum of its last kDwBlock rows plus a compensated (TwoSum) FP32 pair
+// into which each block sum is folded, all in registers, while it walks its
+// chunk (error <= (kDwBlock - 1) ulp of the summed magnitudes).
 // Rows stream through a ring of shared-memory stages filled with cp.async:
 // every thread copies exactly the 16-byte (or 4-byte) pieces of g, x
 // (g_residual) and rstd that it will itself consume, D rows ahead, and waits
@@ -41,6 +43,39 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+
+// Rows summed plainly per column before each compensated fold.
+constexpr int kDwBlock = 8;
+
+// VEC BF16 values from a 16-byte (4-byte) aligned shared-memory slot in one
+// access; zeros when !ok.
+template <int VEC>
+__device__ __forceinline__ BVec<VEC> ld_smem_vec(const unsigned char *p, bool ok)
+{
+    BVec<VEC> v;
+    if constexpr (VEC == 8) {
+        const uint4 u = ok ? *reinterpret_cast<const uint4 *>(p) : make_uint4(0u, 0u, 0u, 0u);
+        v.w[0] = u.x; v.w[1] = u.y; v.w[2] = u.z; v.w[3] = u.w;
+    } else {
+        v.w[0] = ok ? *reinterpret_cast<const uint32_t *>(p) : 0u;
+    }
+    return v;
+}
+
+// VEC FP32 values from shared memory in 16-byte (8-byte) accesses.
+template <int VEC>
+__device__ __forceinline__ void ld_smem_f32(const float *p, bool ok, float (&f)[VEC])
+{
+    if constexpr (VEC == 8) {
+        const float4 a = ok ? *reinterpret_cast<const float4 *>(p) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 b = ok ? *reinterpret_cast<const float4 *>(p + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    } else {
+        const float2 a = ok ? *reinterpret_cast<const float2 *>(p) : make_float2(0.f, 0.f);
+        f[0] = a.x; f[1] = a.y;
+    }
+}
 
 // Bytes of one ring stage: NT tensors x VPT vectors per thread, plus one
 // private rstd slot per thread.
@@ -138,11 +173,23 @@ k_rmsnorm_bwd(const BwdParams p)
     }
     if (rpc > 1) __syncthreads();
 
-    float acc[VPT][VEC], cmp[VPT][VEC];
+    float acc[VPT][VEC], cmp[VPT][VEC], blk[VPT][VEC];
 #pragma unroll
     for (int k = 0; k < VPT; ++k)
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) { acc[k][i] = 0.f; cmp[k][i] = 0.f; }
+        for (int i = 0; i < VEC; ++i) { acc[k][i] = 0.f; cmp[k][i] = 0.f; blk[k][i] = 0.f; }
+    auto fold = [&]() {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) {
+                float s2, err;
+                two_sum(acc[k][i], blk[k][i], s2, err);
+                acc[k][i] = s2;
+                cmp[k][i] = __fadd_rn(cmp[k][i], err);
+                blk[k][i] = 0.f;
+            }
+    };
 
     for (int64_t it = 0; it < iters; ++it) {
         const int64_t t = r0 + grp + it * rpc;
@@ -157,15 +204,10 @@ k_rmsnorm_bwd(const BwdParams p)
         for (int k = 0; k < VPT; ++k) {
             const int v = k * tpr + lane;
             const bool ok = live && v < nvec;
-#pragma unroll
-            for (int i = 0; i < NW; ++i) {
-                gc[k].w[i] = ok ? reinterpret_cast<const uint32_t *>(slot(stage, 0, k))[i] : 0u;
-                xc[k].w[i] = ok ? reinterpret_cast<const uint32_t *>(slot(stage, 1, k))[i] : 0u;
-                if constexpr (GRES)
-                    rc[k].w[i] = ok ? reinterpret_cast<const uint32_t *>(slot(stage, 2, k))[i] : 0u;
-            }
-#pragma unroll
-            for (int i = 0; i < VEC; ++i) we[k][i] = (v < nvec) ? wsm[v * VEC + i] : 0.f;
+            gc[k] = ld_smem_vec<VEC>(slot(stage, 0, k), ok);
+            xc[k] = ld_smem_vec<VEC>(slot(stage, 1, k), ok);
+            if constexpr (GRES) rc[k] = ld_smem_vec<VEC>(slot(stage, 2, k), ok);
+            ld_smem_f32<VEC>(wsm + v * VEC, v < nvec, we[k]);
         }
         const float rs = live ? *rslot(stage) : 0.f;
 
@@ -187,10 +229,7 @@ k_rmsnorm_bwd(const BwdParams p)
             const int warp = threadIdx.x >> 5;
             if ((threadIdx.x & 31) == 0) { red_h[warp] = dh; red_l[warp] = dl; }
             __syncthreads();
-            const int w0 = grp * nwarp;
-            dh = red_h[w0];
-            dl = red_l[w0];
-            for (int i = 1; i < nwarp; ++i) pair_add(dh, dl, red_h[w0 + i], red_l[w0 + i]);
+            pair_reduce_warps(dh, dl, red_h, red_l, grp * nwarp, nwarp);
             __syncthreads();   // red_* is rewritten by the next row
         }
         const float m = __fdiv_rn(__fadd_rn(dh, dl), (float)p.H);
@@ -210,17 +249,9 @@ k_rmsnorm_bwd(const BwdParams p)
                     d[2 * i] = __fadd_rn(d[2 * i], bf_lo(rc[k].w[i]));
                     d[2 * i + 1] = __fadd_rn(d[2 * i + 1], bf_hi(rc[k].w[i]));
                 }
-                // dw term g*x*rstd: g*x is exact in FP32; TwoSum keeps the
-                // accumulation error in cmp.
-                const float e0 = __fmul_rn(__fmul_rn(g0, x0), rs);
-                const float e1 = __fmul_rn(__fmul_rn(g1, x1), rs);
-                float s, err;
-                two_sum(acc[k][2 * i], e0, s, err);
-                acc[k][2 * i] = s;
-                cmp[k][2 * i] = __fadd_rn(cmp[k][2 * i], err);
-                two_sum(acc[k][2 * i + 1], e1, s, err);
-                acc[k][2 * i + 1] = s;
-                cmp[k][2 * i + 1] = __fadd_rn(cmp[k][2 * i + 1], err);
+                // dw term g*x*rstd (g*x is exact in FP32) into the block sum.
+                blk[k][2 * i] = __fadd_rn(blk[k][2 * i], __fmul_rn(__fmul_rn(g0, x0), rs));
+                blk[k][2 * i + 1] = __fadd_rn(blk[k][2 * i + 1], __fmul_rn(__fmul_rn(g1, x1), rs));
             }
             if (live && v < nvec) {
                 BVec<VEC> o;
@@ -229,7 +260,9 @@ k_rmsnorm_bwd(const BwdParams p)
                 st_stream<VEC>(p.dx + t * p.lddx + (int64_t)v * VEC, o);
             }
         }
+        if ((it + 1) % kDwBlock == 0) fold();
     }
+    fold();
     cp_async_wait<0>();
 
     // Combine the CTA's row groups in group order, then write the partial row.
@@ -294,7 +327,7 @@ cudaError_t launch_bwd_inst(BwdParams p, int sms, int *nchunk_out, cudaStream_t 
     const int threads = p.tpr * p.rpc;
     const size_t smem = bwd_smem_bytes(GRES, VEC, VPT, threads, p.rpc, p.H, D);
     auto kern = k_rmsnorm_bwd<W32, GRES, VEC, VPT, SUB, D>;
-    if (smem > 48 * 1024) {
+    if (smem > 46 * 1024) {   // the static reduction arrays share the default 48 KB
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
     }

@@ -130,13 +130,9 @@ k_rmsnorm_fwd(const FwdParams p)
             red_l[warp] = sl_;
         }
         __syncthreads();
-        // Fixed order over the group's warps: every thread of the group gets
-        // the same pair.
-        const int w0 = grp * nwarp;
-        sh_ = red_h[w0];
-        sl_ = red_l[w0];
-        for (int i = 1; i < nwarp; ++i)
-            pair_add(sh_, sl_, red_h[w0 + i], red_l[w0 + i]);
+        // Fixed butterfly over the group's warps: every thread of the group
+        // gets the same pair.
+        pair_reduce_warps(sh_, sl_, red_h, red_l, grp * nwarp, nwarp);
     }
     const float ssum = __fadd_rn(sh_, sl_);
     const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ssum, (float)p.H), p.eps)));
