@@ -9,9 +9,10 @@
 // Design (GB300).  CTA c owns the contiguous row chunk [c*T/n, (c+1)*T/n) of
 // a fixed chunk table (n = chunks, a function of T and the SM count).  Each
 // thread owns the same columns in every row and keeps, per column, a plain
-// FP32 sum of its last kDwBlock rows plus a compensated (TwoSum) FP32 pair
-// into which each block sum is folded, all in registers, while it walks its
-// chunk (error <= (kDwBlock - 1) ulp of the summed magnitudes).
+// FP32 sum (one fused multiply-add per row) of its last kDwBlock rows plus a
+// compensated (TwoSum) FP32 pair into which each block sum is folded, all in
+// registers, while it walks its chunk (error <= kDwBlock ulp of the summed
+// magnitudes).  Elementwise arithmetic uses packed FP32x2 instructions.
 // Rows stream through a ring of shared-memory stages filled with cp.async:
 // every thread copies exactly the 16-byte (or 4-byte) pieces of g, x
 // (g_residual) and rstd that it will itself consume, D rows ahead, and waits
@@ -21,6 +22,8 @@
 // writes one FP32 partial row; a second kernel (bwd_reduce.cu) adds the
 // partial rows of each column in chunk order.
 #pragma once
+
+#include <atomic>
 
 #include "launch.h"
 
@@ -62,18 +65,18 @@ __device__ __forceinline__ BVec<VEC> ld_smem_vec(const unsigned char *p, bool ok
     return v;
 }
 
-// VEC FP32 values from shared memory in 16-byte (8-byte) accesses.
+// VEC FP32 values from shared memory as VEC/2 pairs, in 16-byte (8-byte)
+// accesses; zeros when !ok.
 template <int VEC>
-__device__ __forceinline__ void ld_smem_f32(const float *p, bool ok, float (&f)[VEC])
+__device__ __forceinline__ void ld_smem_f2(const float *p, bool ok, F2 (&f)[VEC / 2])
 {
     if constexpr (VEC == 8) {
         const float4 a = ok ? *reinterpret_cast<const float4 *>(p) : make_float4(0.f, 0.f, 0.f, 0.f);
         const float4 b = ok ? *reinterpret_cast<const float4 *>(p + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
-        f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+        f[0] = f2(a.x, a.y); f[1] = f2(a.z, a.w); f[2] = f2(b.x, b.y); f[3] = f2(b.z, b.w);
     } else {
         const float2 a = ok ? *reinterpret_cast<const float2 *>(p) : make_float2(0.f, 0.f);
-        f[0] = a.x; f[1] = a.y;
+        f[0] = f2(a.x, a.y);
     }
 }
 
@@ -92,7 +95,7 @@ k_rmsnorm_bwd(const BwdParams p)
     constexpr int NT = GRES ? 3 : 2;
     constexpr int S = D + 1;                  // ring stages
     constexpr int VB = VEC * 2;               // bytes per vector
-    __shared__ float red_h[32], red_l[32];
+    __shared__ float red_h[kBwdMaxThreads], red_l[kBwdMaxThreads], tot_h[32], tot_l[32];
     extern __shared__ __align__(16) unsigned char dyn_smem[];
 
     const int nthr = blockDim.x;
@@ -173,22 +176,30 @@ k_rmsnorm_bwd(const BwdParams p)
     }
     if (rpc > 1) __syncthreads();
 
-    float acc[VPT][VEC], cmp[VPT][VEC], blk[VPT][VEC];
+    float acc[VPT][VEC], cmp[VPT][VEC];
+    F2 blk[VPT][NW];
 #pragma unroll
-    for (int k = 0; k < VPT; ++k)
+    for (int k = 0; k < VPT; ++k) {
 #pragma unroll
-        for (int i = 0; i < VEC; ++i) { acc[k][i] = 0.f; cmp[k][i] = 0.f; blk[k][i] = 0.f; }
+        for (int i = 0; i < VEC; ++i) { acc[k][i] = 0.f; cmp[k][i] = 0.f; }
+#pragma unroll
+        for (int i = 0; i < NW; ++i) blk[k][i] = f2(0.f);
+    }
     auto fold = [&]() {
 #pragma unroll
         for (int k = 0; k < VPT; ++k)
 #pragma unroll
             for (int i = 0; i < VEC; ++i) {
+                const float b = (i & 1) ? f2_hi(blk[k][i >> 1]) : f2_lo(blk[k][i >> 1]);
                 float s2, err;
-                two_sum(acc[k][i], blk[k][i], s2, err);
+                two_sum(acc[k][i], b, s2, err);
                 acc[k][i] = s2;
                 cmp[k][i] = __fadd_rn(cmp[k][i], err);
-                blk[k][i] = 0.f;
             }
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+#pragma unroll
+            for (int i = 0; i < NW; ++i) blk[k][i] = f2(0.f);
     };
 
     for (int64_t it = 0; it < iters; ++it) {
@@ -199,7 +210,6 @@ k_rmsnorm_bwd(const BwdParams p)
         cp_async_wait<D>();                  // this thread's copies of row `it` landed
 
         BVec<VEC> gc[VPT], xc[VPT], rc[VPT];
-        float we[VPT][VEC];
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = k * tpr + lane;
@@ -207,58 +217,49 @@ k_rmsnorm_bwd(const BwdParams p)
             gc[k] = ld_smem_vec<VEC>(slot(stage, 0, k), ok);
             xc[k] = ld_smem_vec<VEC>(slot(stage, 1, k), ok);
             if constexpr (GRES) rc[k] = ld_smem_vec<VEC>(slot(stage, 2, k), ok);
-            ld_smem_f32<VEC>(wsm + v * VEC, v < nvec, we[k]);
         }
         const float rs = live ? *rslot(stage) : 0.f;
 
-        // m = mean(g * w * x): FP32 per thread, compensated across threads.
-        float dot = 0.f;
+        // m = mean(g * w * x): FP32 per thread (two lanes), compensated across
+        // threads.
+        F2 dot2 = f2(0.f);
 #pragma unroll
-        for (int k = 0; k < VPT; ++k)
+        for (int k = 0; k < VPT; ++k) {
+            const int v = k * tpr + lane;
+            F2 we[NW];
+            ld_smem_f2<VEC>(wsm + v * VEC, v < nvec, we);
 #pragma unroll
-            for (int i = 0; i < NW; ++i) {
-                dot = __fmaf_rn(__fmul_rn(bf_lo(gc[k].w[i]), we[k][2 * i]), bf_lo(xc[k].w[i]), dot);
-                dot = __fmaf_rn(__fmul_rn(bf_hi(gc[k].w[i]), we[k][2 * i + 1]), bf_hi(xc[k].w[i]), dot);
-            }
-        float dh = dot, dl = 0.f;
-        if constexpr (SUB) {
-            pair_reduce_lanes(dh, dl, tpr);
-        } else {
-            pair_reduce_lanes(dh, dl, 32);
-            const int nwarp = tpr >> 5;
-            const int warp = threadIdx.x >> 5;
-            if ((threadIdx.x & 31) == 0) { red_h[warp] = dh; red_l[warp] = dl; }
-            __syncthreads();
-            pair_reduce_warps(dh, dl, red_h, red_l, grp * nwarp, nwarp);
-            __syncthreads();   // red_* is rewritten by the next row
+            for (int i = 0; i < NW; ++i)
+                dot2 = f2_fma(f2_mul(f2_bf16(gc[k].w[i]), we[i]), f2_bf16(xc[k].w[i]), dot2);
         }
+        float dh, dl;
+        two_sum(f2_lo(dot2), f2_hi(dot2), dh, dl);
+        if constexpr (SUB)
+            pair_reduce_lanes(dh, dl, tpr);
+        else
+            group_sum_pair(dh, dl, red_h, red_l, tot_h, tot_l, grp, tpr);
         const float m = __fdiv_rn(__fadd_rn(dh, dl), (float)p.H);
-        const float c3 = __fmul_rn(__fmul_rn(__fmul_rn(rs, rs), rs), m);
+        const F2 rs2 = f2(rs);
+        const F2 nc3 = f2(-__fmul_rn(__fmul_rn(__fmul_rn(rs, rs), rs), m));
 
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = k * tpr + lane;
-            float d[VEC];
+            F2 we[NW];
+            ld_smem_f2<VEC>(wsm + v * VEC, v < nvec, we);
+            BVec<VEC> o;
 #pragma unroll
             for (int i = 0; i < NW; ++i) {
-                const float g0 = bf_lo(gc[k].w[i]), g1 = bf_hi(gc[k].w[i]);
-                const float x0 = bf_lo(xc[k].w[i]), x1 = bf_hi(xc[k].w[i]);
-                d[2 * i] = __fmaf_rn(-x0, c3, __fmul_rn(rs, __fmul_rn(g0, we[k][2 * i])));
-                d[2 * i + 1] = __fmaf_rn(-x1, c3, __fmul_rn(rs, __fmul_rn(g1, we[k][2 * i + 1])));
-                if constexpr (GRES) {
-                    d[2 * i] = __fadd_rn(d[2 * i], bf_lo(rc[k].w[i]));
-                    d[2 * i + 1] = __fadd_rn(d[2 * i + 1], bf_hi(rc[k].w[i]));
-                }
+                const F2 g2 = f2_bf16(gc[k].w[i]);
+                const F2 x2 = f2_bf16(xc[k].w[i]);
+                // dx = rstd*(g*w) - x*(rstd^3*m) (+ g_residual)
+                F2 d2 = f2_fma(x2, nc3, f2_mul(rs2, f2_mul(g2, we[i])));
+                if constexpr (GRES) d2 = f2_add(d2, f2_bf16(rc[k].w[i]));
+                o.w[i] = bf16_f2(d2);
                 // dw term g*x*rstd (g*x is exact in FP32) into the block sum.
-                blk[k][2 * i] = __fadd_rn(blk[k][2 * i], __fmul_rn(__fmul_rn(g0, x0), rs));
-                blk[k][2 * i + 1] = __fadd_rn(blk[k][2 * i + 1], __fmul_rn(__fmul_rn(g1, x1), rs));
+                blk[k][i] = f2_fma(f2_mul(g2, x2), rs2, blk[k][i]);
             }
-            if (live && v < nvec) {
-                BVec<VEC> o;
-#pragma unroll
-                for (int i = 0; i < NW; ++i) o.w[i] = pack_bf16(d[2 * i], d[2 * i + 1]);
-                st_stream<VEC>(p.dx + t * p.lddx + (int64_t)v * VEC, o);
-            }
+            if (live && v < nvec) st_stream<VEC>(p.dx + t * p.lddx + (int64_t)v * VEC, o);
         }
         if ((it + 1) % kDwBlock == 0) fold();
     }
@@ -327,9 +328,13 @@ cudaError_t launch_bwd_inst(BwdParams p, int sms, int *nchunk_out, cudaStream_t 
     const int threads = p.tpr * p.rpc;
     const size_t smem = bwd_smem_bytes(GRES, VEC, VPT, threads, p.rpc, p.H, D);
     auto kern = k_rmsnorm_bwd<W32, GRES, VEC, VPT, SUB, D>;
-    if (smem > 46 * 1024) {   // the static reduction arrays share the default 48 KB
+    // Opt in to more than the default dynamic shared memory once per kernel
+    // (the largest size requested so far is remembered).
+    static std::atomic<int> opted{0};
+    if ((int)smem > opted.load(std::memory_order_relaxed)) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
+        opted.store((int)smem, std::memory_order_relaxed);
     }
     int per_sm = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);

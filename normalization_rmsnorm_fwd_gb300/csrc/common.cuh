@@ -39,6 +39,57 @@ __device__ __forceinline__ uint32_t pack_fp8(float lo, float hi)
     return r;
 }
 
+// ------------------------------------------------------ packed FP32 pairs --
+// Blackwell executes two FP32 operations per instruction on a 64-bit register
+// pair (add/mul/fma .rn.f32x2); each lane rounds exactly like the scalar
+// IEEE operation, so these only halve the instruction count.
+
+struct F2 {
+    unsigned long long v;
+};
+
+__device__ __forceinline__ F2 f2(float lo, float hi)
+{
+    F2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ F2 f2(float a) { return f2(a, a); }
+__device__ __forceinline__ float f2_lo(F2 a)
+{
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+    return lo;
+}
+__device__ __forceinline__ float f2_hi(F2 a)
+{
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+    return hi;
+}
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b)
+{
+    F2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+__device__ __forceinline__ F2 f2_mul(F2 a, F2 b)
+{
+    F2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+__device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c)
+{
+    F2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+    return r;
+}
+// Packed BF16 pair -> FP32 pair (exact).
+__device__ __forceinline__ F2 f2_bf16(uint32_t w) { return f2(bf_lo(w), bf_hi(w)); }
+// FP32 pair -> packed BF16 pair, round to nearest even.
+__device__ __forceinline__ uint32_t bf16_f2(F2 a) { return pack_bf16(f2_lo(a), f2_hi(a)); }
+
 // ------------------------------------------------------------ vectors ----
 // VEC BF16 elements = VEC/2 packed words.  VEC is 8 (16-byte accesses) or 2
 // (4-byte accesses).
@@ -160,6 +211,51 @@ __device__ __forceinline__ void pair_reduce_warps(float &h, float &l, const floa
     h = i < nwarp ? red_h[w0 + i] : 0.f;
     l = i < nwarp ? red_l[w0 + i] : 0.f;
     pair_reduce_lanes(h, l, width);
+}
+
+// (h, l) += (bh, bl) without renormalisation (cascaded "Sum2"): the TwoSum
+// error of the leading parts joins the trailing parts.  Symmetric in its two
+// operands, so butterfly partners stay bit-identical.
+__device__ __forceinline__ void pair_acc(float &h, float &l, float bh, float bl)
+{
+    float s, e;
+    two_sum(h, bh, s, e);
+    h = s;
+    l = __fadd_rn(__fadd_rn(l, bl), e);
+}
+
+// Sum of the pairs (h, l) of the tpr threads of a multi-warp row group,
+// returned to every thread of the group.  Every thread stores its pair; the
+// first warp of the group adds the pairs of threads lane, lane+32, ... in
+// that order, then the 32 lane sums in a butterfly, and publishes the total.
+// red_h / red_l hold one slot per thread of the CTA, tot_h / tot_l one per
+// group.  Two CTA barriers; the fixed order makes the result bitwise
+// reproducible.
+__device__ __forceinline__ void group_sum_pair(float &h, float &l, float *red_h, float *red_l,
+                                               float *tot_h, float *tot_l, int grp, int tpr)
+{
+    red_h[threadIdx.x] = h;
+    red_l[threadIdx.x] = l;
+    __syncthreads();
+    const int lane32 = threadIdx.x & 31;
+    const int base = grp * tpr;
+    if (threadIdx.x - base < 32) {
+        h = red_h[base + lane32];
+        l = red_l[base + lane32];
+        for (int j = lane32 + 32; j < tpr; j += 32) pair_acc(h, l, red_h[base + j], red_l[base + j]);
+        for (int o = 16; o > 0; o >>= 1) {
+            const float bh = __shfl_xor_sync(0xffffffffu, h, o);
+            const float bl = __shfl_xor_sync(0xffffffffu, l, o);
+            pair_acc(h, l, bh, bl);
+        }
+        if (lane32 == 0) {
+            tot_h[grp] = h;
+            tot_l[grp] = l;
+        }
+    }
+    __syncthreads();
+    h = tot_h[grp];
+    l = tot_l[grp];
 }
 
 }  // namespace crmsn

@@ -14,6 +14,7 @@
 // "flashrt-adaptive-norms" README formula block):
 //   h      = x | bf16(x + residual) | bf16(residual + bf16(x * gate))
 //   ss     = sum h^2 (FP32 per thread, compensated pairs across threads)
+//   (elementwise FP32 arithmetic in packed FP32x2 instructions)
 //   rstd   = 1 / sqrt(ss / H + eps)        (IEEE sqrt and division)
 //   o      = (h * rstd) * f32(w + bias)
 //   then one of the epilogues below.
@@ -82,7 +83,7 @@ k_rmsnorm_fwd(const FwdParams p)
 
     // ---------------- phase 2: normalised input h, sum of squares ---------
     BVec<VEC> h[VPT];
-    float ss = 0.f;
+    F2 ss2 = f2(0.f);
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
 #pragma unroll
@@ -94,21 +95,17 @@ k_rmsnorm_fwd(const FwdParams p)
             } else if constexpr (IN == IN_RESIDUAL) {
                 // The FP32 sum of two BF16 values rounded once to BF16 is the
                 // correctly rounded BF16 sum (double rounding is innocuous).
-                const uint32_t rw = ra[k].w[i];
-                hw = pack_bf16(__fadd_rn(bf_lo(xw), bf_lo(rw)), __fadd_rn(bf_hi(xw), bf_hi(rw)));
+                hw = bf16_f2(f2_add(f2_bf16(xw), f2_bf16(ra[k].w[i])));
             } else {
                 // bf16(x * gate) first (the FP32 product of two BF16 values is
                 // exact), then the BF16 residual add.
-                const uint32_t gw = ga[k].w[i];
-                const uint32_t pw = pack_bf16(__fmul_rn(bf_lo(xw), bf_lo(gw)),
-                                              __fmul_rn(bf_hi(xw), bf_hi(gw)));
-                const uint32_t rw = ra[k].w[i];
-                hw = pack_bf16(__fadd_rn(bf_lo(rw), bf_lo(pw)), __fadd_rn(bf_hi(rw), bf_hi(pw)));
+                const uint32_t pw = bf16_f2(f2_mul(f2_bf16(xw), f2_bf16(ga[k].w[i])));
+                hw = bf16_f2(f2_add(f2_bf16(ra[k].w[i]), f2_bf16(pw)));
             }
             h[k].w[i] = hw;
-            // h^2 is exact in FP32, so fma rounds only the accumulation.
-            ss = __fmaf_rn(bf_lo(hw), bf_lo(hw), ss);
-            ss = __fmaf_rn(bf_hi(hw), bf_hi(hw), ss);
+            // h^2 is exact in FP32, so the fma rounds only the accumulation.
+            const F2 h2 = f2_bf16(hw);
+            ss2 = f2_fma(h2, h2, ss2);
         }
         if constexpr (IN != IN_PLAIN) {
             const int v = k * tpr + lane;
@@ -118,10 +115,13 @@ k_rmsnorm_fwd(const FwdParams p)
     }
 
     // ---------------- phase 3: row reduction -> rstd ----------------------
-    float sh_ = ss, sl_ = 0.f;
+    float sh_, sl_;
+    two_sum(f2_lo(ss2), f2_hi(ss2), sh_, sl_);
     if constexpr (SUB) {
         pair_reduce_lanes(sh_, sl_, tpr);
     } else {
+        // Butterfly within each warp, then across the group's warps: short
+        // latency for these short-lived CTAs.
         pair_reduce_lanes(sh_, sl_, 32);
         const int nwarp = tpr >> 5;
         const int warp = threadIdx.x >> 5;
@@ -130,8 +130,6 @@ k_rmsnorm_fwd(const FwdParams p)
             red_l[warp] = sl_;
         }
         __syncthreads();
-        // Fixed butterfly over the group's warps: every thread of the group
-        // gets the same pair.
         pair_reduce_warps(sh_, sl_, red_h, red_l, grp * nwarp, nwarp);
     }
     const float ssum = __fadd_rn(sh_, sl_);
@@ -143,38 +141,31 @@ k_rmsnorm_fwd(const FwdParams p)
     float scale_v = 1.f;
     if constexpr (OUT == OUT_Q || OUT == OUT_ADA_Q)
         scale_v = __ldg(p.scale);
+    const F2 rstd2 = f2(rstd);
+    const F2 bias2 = f2(p.bias);
 
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = k * tpr + lane;
         const bool ok = live && v < nvec;
         const int64_t c = (int64_t)v * VEC;
-        float o[VEC];
+        F2 o[NW];
 #pragma unroll
         for (int i = 0; i < NW; ++i) {
-            float we0, we1;
-            if constexpr (W32) {
-                we0 = __fadd_rn(wf[k][2 * i], p.bias);
-                we1 = __fadd_rn(wf[k][2 * i + 1], p.bias);
-            } else {
-                we0 = __fadd_rn(bf_lo(wb[k].w[i]), p.bias);
-                we1 = __fadd_rn(bf_hi(wb[k].w[i]), p.bias);
-            }
-            o[2 * i] = __fmul_rn(__fmul_rn(bf_lo(h[k].w[i]), rstd), we0);
-            o[2 * i + 1] = __fmul_rn(__fmul_rn(bf_hi(h[k].w[i]), rstd), we1);
+            const F2 w2 = W32 ? f2(wf[k][2 * i], wf[k][2 * i + 1]) : f2_bf16(wb[k].w[i]);
+            o[i] = f2_mul(f2_mul(f2_bf16(h[k].w[i]), rstd2), f2_add(w2, bias2));
         }
 
         if constexpr (OUT == OUT_Y) {
             BVec<VEC> yv;
 #pragma unroll
-            for (int i = 0; i < NW; ++i) yv.w[i] = pack_bf16(o[2 * i], o[2 * i + 1]);
+            for (int i = 0; i < NW; ++i) yv.w[i] = bf16_f2(o[i]);
             if (ok) st_stream<VEC>(p.y + t * p.ldy + c, yv);
         } else if constexpr (OUT == OUT_Q) {
             uint32_t cq[NW];
 #pragma unroll
             for (int i = 0; i < NW; ++i)
-                cq[i] = pack_fp8<FP8K>(__fdiv_rn(o[2 * i], scale_v),
-                                       __fdiv_rn(o[2 * i + 1], scale_v));
+                cq[i] = pack_fp8<FP8K>(__fdiv_rn(f2_lo(o[i]), scale_v), __fdiv_rn(f2_hi(o[i]), scale_v));
             if (ok) st_fp8<VEC>(p.q + t * p.ldq + c, cq);
         } else if constexpr (OUT == OUT_BLOCK) {
             // normed = bf16(o); amax over the 128-column block held by 16
@@ -183,7 +174,7 @@ k_rmsnorm_fwd(const FwdParams p)
             float amax = 0.f;
 #pragma unroll
             for (int i = 0; i < NW; ++i) {
-                nv.w[i] = pack_bf16(o[2 * i], o[2 * i + 1]);
+                nv.w[i] = bf16_f2(o[i]);
                 amax = fmaxf(amax, fmaxf(fabsf(bf_lo(nv.w[i])), fabsf(bf_hi(nv.w[i]))));
             }
             if (ok) st_stream<VEC>(p.y + t * p.ldy + c, nv);
@@ -204,24 +195,22 @@ k_rmsnorm_fwd(const FwdParams p)
                 if ((v & 15) == 0)
                     p.bscale[(int64_t)(v >> 4) * p.ldT + t] = s;
             }
-        } else {  // ADA
-            float ov[VEC];
+        } else {  // ADA: o * (1 + scale) + shift, one FP32 rounding (fma)
+            const F2 one2 = f2(1.f);
+            F2 ov[NW];
 #pragma unroll
-            for (int i = 0; i < NW; ++i) {
-                ov[2 * i] = __fmaf_rn(o[2 * i], __fadd_rn(1.f, bf_lo(sc[k].w[i])), bf_lo(sh[k].w[i]));
-                ov[2 * i + 1] = __fmaf_rn(o[2 * i + 1], __fadd_rn(1.f, bf_hi(sc[k].w[i])), bf_hi(sh[k].w[i]));
-            }
+            for (int i = 0; i < NW; ++i)
+                ov[i] = f2_fma(o[i], f2_add(one2, f2_bf16(sc[k].w[i])), f2_bf16(sh[k].w[i]));
             if constexpr (OUT == OUT_ADA) {
                 BVec<VEC> out;
 #pragma unroll
-                for (int i = 0; i < NW; ++i) out.w[i] = pack_bf16(ov[2 * i], ov[2 * i + 1]);
+                for (int i = 0; i < NW; ++i) out.w[i] = bf16_f2(ov[i]);
                 if (ok) st_stream<VEC>(p.y + t * p.ldy + c, out);
             } else {
                 uint32_t cq[NW];
 #pragma unroll
                 for (int i = 0; i < NW; ++i)
-                    cq[i] = pack_fp8<0>(__fdiv_rn(ov[2 * i], scale_v),
-                                        __fdiv_rn(ov[2 * i + 1], scale_v));
+                    cq[i] = pack_fp8<0>(__fdiv_rn(f2_lo(ov[i]), scale_v), __fdiv_rn(f2_hi(ov[i]), scale_v));
                 if (ok) st_fp8<VEC>(p.q + t * p.ldq + c, cq);
             }
             if (ok) st_stream<VEC>(p.gate_out + t * p.ldgo + c, gt[k]);
