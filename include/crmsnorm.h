@@ -61,7 +61,8 @@ typedef enum crmsn_status {
     CRMSN_ERR_ALIAS = 7,          /* outputs overlap inputs other than as allowed */
     CRMSN_ERR_CUDA = 8,           /* the CUDA runtime reported an error */
     CRMSN_ERR_DEVICE_TIMEOUT = 9, /* reserved: the kernels have no device-side waits */
-    CRMSN_ERR_ARG = 10            /* eps / scale value out of range */
+    CRMSN_ERR_ARG = 10,           /* eps / scale value out of range */
+    CRMSN_ERR_SCRATCH_LIMIT = 11  /* rmsnorm_bwd_noalloc: problem needs more than its built-in scratch */
 } crmsn_status;
 
 /* Weight storage types. */
@@ -152,6 +153,33 @@ crmsn_status rmsnorm_bwd(const void *g, int64_t ldg,
  */
 size_t rmsnorm_bwd_workspace_bytes(int64_t rows, int64_t H, int device,
                                    int residual);
+
+/*
+ * rmsnorm_bwd_noalloc -- no counterpart on the pages: the backward of
+ * rmsnorm_bwd for callers that cannot provide a workspace (engines and plugin
+ * hosts that plan all device memory in advance and forbid allocation inside
+ * an operation, or C callers without a device allocator, for whom a
+ * cudaMalloc per call would also stall the device).  Same arguments, results
+ * and dw determinism as rmsnorm_bwd, minus the workspace; allocates nothing.
+ *
+ * The scratch is a 16 MiB array in the library's own device memory, held by
+ * every GPU that loads the library until the process exits.  The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress with
+ * that device current); make that first call before any stream capture.  All
+ * calls on a device share the array: calls that overlap on the GPU (other
+ * streams or host threads) race and must be serialised.  The scratch needs
+ * no zeroing.  Problems whose workspace (rmsnorm_bwd_workspace_bytes) exceeds
+ * 16 MiB -- on a 152-SM GB300, H above about 13,700 -- return
+ * CRMSN_ERR_SCRATCH_LIMIT without launching anything.
+ */
+crmsn_status rmsnorm_bwd_noalloc(const void *g, int64_t ldg,
+                                 const void *x, int64_t ldx,
+                                 const void *w, int w_dtype, float weight_bias,
+                                 const float *rstd,
+                                 const void *g_residual, int64_t ldgr,
+                                 int64_t T, int64_t H,
+                                 void *dx, int64_t lddx, float *dw,
+                                 cudaStream_t stream);
 
 /*
  * fused_add_rmsnorm_quant -- [API] fused_add_rmsnorm_quant and rmsnorm_quant;

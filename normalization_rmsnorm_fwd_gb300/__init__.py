@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     fused_add_rmsnorm_quant,
     gate_residual_ada_norm_fp8,
     rmsnorm_bwd,
+    rmsnorm_bwd_noalloc,
     rmsnorm_bwd_workspace,
     rmsnorm_bwd_workspace_bytes,
     rmsnorm_fwd,

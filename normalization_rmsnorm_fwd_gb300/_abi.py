@@ -22,6 +22,7 @@ SIGNATURES = {
     "rmsnorm_bwd": (_ST, [_P, _I, _P, _I, _P, _INT, _F, _P, _P, _I, _I, _I, _P, _I, _P, _P,
                           ctypes.c_size_t, _P]),
     "rmsnorm_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _INT, _INT]),
+    "rmsnorm_bwd_noalloc": (_ST, [_P, _I, _P, _I, _P, _INT, _F, _P, _P, _I, _I, _I, _P, _I, _P, _P]),
     "fused_add_rmsnorm_quant": (_ST, [_P, _I, _INT, _P, _I, _P, _I, _P, _INT, _F, _P, _F, _I, _I,
                                       _P, _P]),
     "fused_add_rmsnorm_fp8_block_quant": (_ST, [_P, _P, _I, _P, _P, _I, _P, _I, _P, _F, _I, _I,
@@ -36,6 +37,7 @@ STATUS = {
     0: "CRMSN_OK", 1: "CRMSN_ERR_NULL", 2: "CRMSN_ERR_SHAPE", 3: "CRMSN_ERR_UNSUPPORTED_H",
     4: "CRMSN_ERR_ALIGNMENT", 5: "CRMSN_ERR_DTYPE", 6: "CRMSN_ERR_WORKSPACE",
     7: "CRMSN_ERR_ALIAS", 8: "CRMSN_ERR_CUDA", 9: "CRMSN_ERR_DEVICE_TIMEOUT", 10: "CRMSN_ERR_ARG",
+    11: "CRMSN_ERR_SCRATCH_LIMIT",
 }
 OK = 0
 BF16, F32 = 0, 1

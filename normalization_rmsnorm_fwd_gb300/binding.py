@@ -278,5 +278,32 @@ def rmsnorm_bwd(g, x, w, rstd, weight_bias: float = 0.0, g_residual=None, worksp
     return dx, dw
 
 
+def rmsnorm_bwd_noalloc(g, x, w, rstd, weight_bias: float = 0.0, g_residual=None, dx=None,
+                        dw=None):
+    """rmsnorm_bwd for callers that cannot provide a workspace: the library's
+    built-in 16 MiB scratch is used instead, shared by every call on the
+    device (overlapping calls race).  Returns (dx, dw)."""
+    _bf16(g, "g")
+    _bf16(x, "x")
+    kind = _weight(w)
+    T, H, ldx = as_rows(x, "x")
+    _, _, ldg = as_rows(g, "g")
+    ldgr = 0
+    if g_residual is not None:
+        _bf16(g_residual, "g_residual")
+        _, _, ldgr = as_rows(g_residual, "g_residual")
+    if dx is None:
+        dx = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+    _, _, lddx = as_rows(dx, "dx")
+    if dw is None:
+        dw = torch.empty(H, dtype=torch.float32, device=x.device)
+    with torch.cuda.device(x.device):
+        st = _lib().rmsnorm_bwd_noalloc(_ptr(g), ldg, _ptr(x), ldx, _ptr(w), kind,
+                                        float(weight_bias), _ptr(rstd), _ptr(g_residual), ldgr, T,
+                                        H, _ptr(dx), lddx, _ptr(dw), _stream(x))
+    check("rmsnorm_bwd_noalloc", st)
+    return dx, dw
+
+
 def rmsnorm_supports(H: int, w_dtype: int = BF16, op: int = _abi.OP_FWD) -> int:
     return _lib().rmsnorm_supports(int(H), int(w_dtype), int(op))

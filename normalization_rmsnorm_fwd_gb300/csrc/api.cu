@@ -246,6 +246,7 @@ const char *crmsn_status_str(crmsn_status s)
         case CRMSN_ERR_CUDA: return "CUDA runtime error";
         case CRMSN_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
         case CRMSN_ERR_ARG: return "eps or scale out of range";
+        case CRMSN_ERR_SCRATCH_LIMIT: return "problem needs more than the built-in 16 MiB backward scratch";
     }
     return "unknown status";
 }

@@ -14,7 +14,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADERS = [os.path.join(ROOT, "include", f) for f in os.listdir(os.path.join(ROOT, "include"))
            if f.endswith(".h")]
 
-OK, NULL, SHAPE, UNSUP, ALIGN, DTYPE, WS, ALIAS, CUDA, TIMEOUT, ARG = range(11)
+OK, NULL, SHAPE, UNSUP, ALIGN, DTYPE, WS, ALIAS, CUDA, TIMEOUT, ARG, SCRATCH = range(12)
 A = 1 << 40            # a fake, 256-byte aligned device address (never dereferenced)
 MB = 1 << 20
 
@@ -47,7 +47,7 @@ def test_every_declared_symbol_is_exported(L):
 
 
 def test_status_strings(L):
-    for s in range(11):
+    for s in range(12):
         assert L.crmsn_status_str(s)
     assert L.crmsn_status_str(99) == b"unknown status"
 

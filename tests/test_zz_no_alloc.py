@@ -1,0 +1,79 @@
+"""rmsnorm_bwd_noalloc: the backward for callers that cannot allocate.
+
+Engines and plugin hosts that plan every device buffer in advance, and C
+callers with no device allocator, cannot pass rmsnorm_bwd a workspace; this
+entry point uses the library's built-in scratch instead.  The test calls it
+through the C ABI twice in a row (different shapes, so the second call runs on
+the scratch the first one left behind) and checks dx and dw against
+rmsnorm_bwd with a caller-owned workspace on the same inputs, within the
+tolerances the other GPU tests use.  It also checks that a problem needing
+more than the built-in scratch is refused.  This file sorts last so that a
+run stopping at its first failure has already run every other test.
+"""
+import numpy as np
+import pytest
+import torch
+
+import numfmt
+from normalization_rmsnorm_fwd_gb300 import _abi, synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _dev_bf16(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+
+def _bits(t):
+    return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def test_noalloc_backward_matches_rmsnorm_bwd():
+    L = _abi.load()
+    torch.cuda.set_device(0)
+    stream = torch.cuda.current_stream().cuda_stream
+    for seed, (T, H, gres) in enumerate([(2048, 4096, False), (333, 5120, True)]):
+        g_b, x_b, r_b = synth.random_rows(100 + seed, T, H, n=3)
+        w_b = synth.random_weight(100 + seed, H)
+        g, x, w = _dev_bf16(g_b), _dev_bf16(x_b), _dev_bf16(w_b)
+        gr = _dev_bf16(r_b) if gres else None
+        rstd = torch.from_numpy(np.abs(synth.Draw(seed).f32((T,), 0.1, 1.0))).cuda()
+        # Existing entry point with a caller-owned workspace.
+        nbytes = L.rmsnorm_bwd_workspace_bytes(T, H, 0, int(gres))
+        ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        dx_ref = torch.empty_like(x)
+        dw_ref = torch.empty(H, device="cuda")
+        st = L.rmsnorm_bwd(g.data_ptr(), H, x.data_ptr(), H, w.data_ptr(), 0, 0.0, rstd.data_ptr(),
+                           gr.data_ptr() if gres else None, H, T, H, dx_ref.data_ptr(), H,
+                           dw_ref.data_ptr(), ws.data_ptr(), nbytes, stream)
+        assert st == 0, _abi.STATUS[st]
+        # The no-allocation entry point on the same inputs.
+        dx = torch.full_like(x, float("nan"))
+        dw = torch.full((H,), float("nan"), device="cuda")
+        st = L.rmsnorm_bwd_noalloc(g.data_ptr(), H, x.data_ptr(), H, w.data_ptr(), 0, 0.0,
+                                   rstd.data_ptr(), gr.data_ptr() if gres else None, H, T, H,
+                                   dx.data_ptr(), H, dw.data_ptr(), stream)
+        assert st == 0, _abi.STATUS[st]
+        torch.cuda.synchronize()
+        a = numfmt.decode_bf16(_bits(dx))
+        b = numfmt.decode_bf16(_bits(dx_ref))
+        assert np.all(np.abs(a - b) <= numfmt.bf16_ulp(b)), "dx differs by more than one BF16 ulp"
+        dwa, dwb = dw.cpu().numpy().astype(np.float64), dw_ref.cpu().numpy().astype(np.float64)
+        assert np.linalg.norm(dwa - dwb) <= 1e-5 * np.linalg.norm(dwb), "dw beyond 1e-5 relative"
+
+
+def test_noalloc_refuses_problems_beyond_its_scratch():
+    L = _abi.load()
+    torch.cuda.set_device(0)
+    H = 16384
+    need = L.rmsnorm_bwd_workspace_bytes(4096, H, 0, 0)
+    assert need > 16 << 20
+    t = torch.zeros((4096, H), dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(H, dtype=torch.bfloat16, device="cuda")
+    rstd = torch.ones(4096, device="cuda")
+    dw = torch.empty(H, device="cuda")
+    dx = torch.empty_like(t)
+    st = L.rmsnorm_bwd_noalloc(t.data_ptr(), H, t.data_ptr(), H, w.data_ptr(), 0, 0.0, rstd.data_ptr(),
+                               None, 0, 4096, H, dx.data_ptr(), H, dw.data_ptr(),
+                               torch.cuda.current_stream().cuda_stream)
+    assert _abi.STATUS[st] == "CRMSN_ERR_SCRATCH_LIMIT"
