@@ -51,31 +51,31 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 constexpr int kDwBlock = 8;
 
 // VEC BF16 values from a 16-byte (4-byte) aligned shared-memory slot in one
-// access; zeros when !ok.
+// access.
 template <int VEC>
-__device__ __forceinline__ BVec<VEC> ld_smem_vec(const unsigned char *p, bool ok)
+__device__ __forceinline__ BVec<VEC> ld_smem_vec(const unsigned char *p)
 {
     BVec<VEC> v;
     if constexpr (VEC == 8) {
-        const uint4 u = ok ? *reinterpret_cast<const uint4 *>(p) : make_uint4(0u, 0u, 0u, 0u);
+        const uint4 u = *reinterpret_cast<const uint4 *>(p);
         v.w[0] = u.x; v.w[1] = u.y; v.w[2] = u.z; v.w[3] = u.w;
     } else {
-        v.w[0] = ok ? *reinterpret_cast<const uint32_t *>(p) : 0u;
+        v.w[0] = *reinterpret_cast<const uint32_t *>(p);
     }
     return v;
 }
 
 // VEC FP32 values from shared memory as VEC/2 pairs, in 16-byte (8-byte)
-// accesses; zeros when !ok.
+// accesses.
 template <int VEC>
-__device__ __forceinline__ void ld_smem_f2(const float *p, bool ok, F2 (&f)[VEC / 2])
+__device__ __forceinline__ void ld_smem_f2(const float *p, F2 (&f)[VEC / 2])
 {
     if constexpr (VEC == 8) {
-        const float4 a = ok ? *reinterpret_cast<const float4 *>(p) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float4 b = ok ? *reinterpret_cast<const float4 *>(p + 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 a = *reinterpret_cast<const float4 *>(p);
+        const float4 b = *reinterpret_cast<const float4 *>(p + 4);
         f[0] = f2(a.x, a.y); f[1] = f2(a.z, a.w); f[2] = f2(b.x, b.y); f[3] = f2(b.z, b.w);
     } else {
-        const float2 a = ok ? *reinterpret_cast<const float2 *>(p) : make_float2(0.f, 0.f);
+        const float2 a = *reinterpret_cast<const float2 *>(p);
         f[0] = f2(a.x, a.y);
     }
 }
@@ -95,7 +95,7 @@ k_rmsnorm_bwd(const BwdParams p)
     constexpr int NT = GRES ? 3 : 2;
     constexpr int S = D + 1;                  // ring stages
     constexpr int VB = VEC * 2;               // bytes per vector
-    __shared__ float red_h[kBwdMaxThreads], red_l[kBwdMaxThreads], tot_h[32], tot_l[32];
+    __shared__ float red_h[2 * kBwdMaxThreads], red_l[2 * kBwdMaxThreads], tot_h[64], tot_l[64];
     extern __shared__ __align__(16) unsigned char dyn_smem[];
 
     const int nthr = blockDim.x;
@@ -108,12 +108,12 @@ k_rmsnorm_bwd(const BwdParams p)
     const int64_t r1 = (int64_t)(blockIdx.x + 1) * p.T / p.nchunk;
     const int64_t iters = (r1 - r0 + rpc - 1) / rpc;
 
-    // Shared memory: ring [S][stage], then w_eff [H], then the row-group
-    // combine area [rpc-1][H][2].
+    // Shared memory: ring [S][stage], then w_eff [VPT*tpr*VEC] (zero past H),
+    // then the row-group combine area [rpc-1][H][2].
     const int stage_bytes = bwd_stage_bytes(NT, VPT, VEC, nthr);
     unsigned char *ring = dyn_smem;
     float *wsm = reinterpret_cast<float *>(dyn_smem + (size_t)S * stage_bytes);
-    float *comb = wsm + p.H;
+    float *comb = wsm + VPT * tpr * VEC;
 
     auto slot = [&](int stage, int tensor, int k) -> unsigned char * {
         return ring + (size_t)stage * stage_bytes + ((size_t)(tensor * VPT + k) * nthr + threadIdx.x) * VB;
@@ -148,17 +148,37 @@ k_rmsnorm_bwd(const BwdParams p)
         cp_async_commit();   // one group per iteration, empty or not
     };
 
-    // Prologue: the first D rows go in flight while the weight is prepared.
+    // Prologue: the first rows go in flight while the weight is prepared
+    // (D rows; D - 1 when multi-warp groups take their rows in pairs).
+    constexpr bool PAIR = !SUB && D >= 1;
+    constexpr int PRO = PAIR ? D - 1 : D;
 #pragma unroll
-    for (int i = 0; i < D; ++i) issue(i);
+    for (int i = 0; i < PRO; ++i) issue(i);
 
     // Effective weight f32(w + bias) of this thread's columns, in shared
     // memory; group 0 writes it, the other groups read it after a barrier.
+    // Columns past H (the last vectors of a row that does not fill the
+    // layout) get a zero weight and zero ring slots, which the copies never
+    // touch, so every shared-memory load below is unconditional and those
+    // columns add exact zeros to m and dw.
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = k * tpr + lane;
-        if (grp == 0 && v < nvec) {
-            const int64_t c = (int64_t)v * VEC;
+        const int64_t c = (int64_t)v * VEC;
+        if (v >= nvec) {
+#pragma unroll
+            for (int st = 0; st < S; ++st)
+#pragma unroll
+                for (int ti = 0; ti < NT; ++ti) {
+                    if constexpr (VEC == 8)
+                        *reinterpret_cast<uint4 *>(slot(st, ti, k)) = make_uint4(0u, 0u, 0u, 0u);
+                    else
+                        *reinterpret_cast<uint32_t *>(slot(st, ti, k)) = 0u;
+                }
+            if (grp == 0)
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) wsm[c + i] = 0.f;
+        } else if (grp == 0) {
             if constexpr (W32) {
                 float f[VEC];
                 ld_f32_keep<VEC>(static_cast<const float *>(p.w) + c, f);
@@ -202,66 +222,93 @@ k_rmsnorm_bwd(const BwdParams p)
             for (int i = 0; i < NW; ++i) blk[k][i] = f2(0.f);
     };
 
-    for (int64_t it = 0; it < iters; ++it) {
-        const int64_t t = r0 + grp + it * rpc;
-        const bool live = t < r1;
-        const int stage = (int)(it % S);
-        issue(it + D);                       // keep D rows ahead in flight
-        cp_async_wait<D>();                  // this thread's copies of row `it` landed
-
-        BVec<VEC> gc[VPT], xc[VPT], rc[VPT];
+    // Row sum of g*w*x over this thread's columns of iteration i's row: FP32
+    // in two lanes, then one TwoSum; zero for an iteration past the chunk.
+    auto row_dot = [&](int64_t i, float &dh, float &dl) {
+        dh = 0.f;
+        dl = 0.f;
+        if (r0 + grp + i * rpc < r1) {
+            const int stage = (int)(i % S);
+            F2 dot2 = f2(0.f);
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int v = k * tpr + lane;
-            const bool ok = live && v < nvec;
-            gc[k] = ld_smem_vec<VEC>(slot(stage, 0, k), ok);
-            xc[k] = ld_smem_vec<VEC>(slot(stage, 1, k), ok);
-            if constexpr (GRES) rc[k] = ld_smem_vec<VEC>(slot(stage, 2, k), ok);
+            for (int k = 0; k < VPT; ++k) {
+                const BVec<VEC> gv = ld_smem_vec<VEC>(slot(stage, 0, k));
+                const BVec<VEC> xv = ld_smem_vec<VEC>(slot(stage, 1, k));
+                F2 we[NW];
+                ld_smem_f2<VEC>(wsm + (k * tpr + lane) * VEC, we);
+#pragma unroll
+                for (int e = 0; e < NW; ++e)
+                    dot2 = f2_fma(f2_mul(f2_bf16(gv.w[e]), we[e]), f2_bf16(xv.w[e]), dot2);
+            }
+            two_sum(f2_lo(dot2), f2_hi(dot2), dh, dl);
         }
-        const float rs = live ? *rslot(stage) : 0.f;
-
-        // m = mean(g * w * x): FP32 per thread (two lanes), compensated across
-        // threads.
-        F2 dot2 = f2(0.f);
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int v = k * tpr + lane;
-            F2 we[NW];
-            ld_smem_f2<VEC>(wsm + v * VEC, v < nvec, we);
-#pragma unroll
-            for (int i = 0; i < NW; ++i)
-                dot2 = f2_fma(f2_mul(f2_bf16(gc[k].w[i]), we[i]), f2_bf16(xc[k].w[i]), dot2);
-        }
-        float dh, dl;
-        two_sum(f2_lo(dot2), f2_hi(dot2), dh, dl);
-        if constexpr (SUB)
-            pair_reduce_lanes(dh, dl, tpr);
-        else
-            group_sum_pair(dh, dl, red_h, red_l, tot_h, tot_l, grp, tpr);
-        const float m = __fdiv_rn(__fadd_rn(dh, dl), (float)p.H);
+    };
+    // dx of iteration i's row and its dw terms, given the row's compensated
+    // sum (sh, sl) of g*w*x.
+    auto row_dx = [&](int64_t i, float sh, float sl) {
+        const int64_t t = r0 + grp + i * rpc;
+        if (t >= r1) return;
+        const int stage = (int)(i % S);
+        const float rs = *rslot(stage);
+        const float m = __fdiv_rn(__fadd_rn(sh, sl), (float)p.H);
         const F2 rs2 = f2(rs);
         const F2 nc3 = f2(-__fmul_rn(__fmul_rn(__fmul_rn(rs, rs), rs), m));
-
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = k * tpr + lane;
+            const BVec<VEC> gv = ld_smem_vec<VEC>(slot(stage, 0, k));
+            const BVec<VEC> xv = ld_smem_vec<VEC>(slot(stage, 1, k));
+            BVec<VEC> rv;
+            if constexpr (GRES) rv = ld_smem_vec<VEC>(slot(stage, 2, k));
             F2 we[NW];
-            ld_smem_f2<VEC>(wsm + v * VEC, v < nvec, we);
+            ld_smem_f2<VEC>(wsm + v * VEC, we);
             BVec<VEC> o;
 #pragma unroll
-            for (int i = 0; i < NW; ++i) {
-                const F2 g2 = f2_bf16(gc[k].w[i]);
-                const F2 x2 = f2_bf16(xc[k].w[i]);
+            for (int e = 0; e < NW; ++e) {
+                const F2 g2 = f2_bf16(gv.w[e]);
+                const F2 x2 = f2_bf16(xv.w[e]);
                 // dx = rstd*(g*w) - x*(rstd^3*m) (+ g_residual)
-                F2 d2 = f2_fma(x2, nc3, f2_mul(rs2, f2_mul(g2, we[i])));
-                if constexpr (GRES) d2 = f2_add(d2, f2_bf16(rc[k].w[i]));
-                o.w[i] = bf16_f2(d2);
+                F2 d2 = f2_fma(x2, nc3, f2_mul(rs2, f2_mul(g2, we[e])));
+                if constexpr (GRES) d2 = f2_add(d2, f2_bf16(rv.w[e]));
+                o.w[e] = bf16_f2(d2);
                 // dw term g*x*rstd (g*x is exact in FP32) into the block sum.
-                blk[k][i] = f2_fma(f2_mul(g2, x2), rs2, blk[k][i]);
+                blk[k][e] = f2_fma(f2_mul(g2, x2), rs2, blk[k][e]);
             }
-            if (live && v < nvec) st_stream<VEC>(p.dx + t * p.lddx + (int64_t)v * VEC, o);
+            if (v < nvec) st_stream<VEC>(p.dx + t * p.lddx + (int64_t)v * VEC, o);
         }
-        if ((it + 1) % kDwBlock == 0) fold();
+    };
+
+    if constexpr (PAIR) {
+        // Multi-warp groups take their rows two at a time: both rows' partial
+        // sums are formed, two warps reduce the two rows at once (half the
+        // barriers and the reduction latency per row), then both rows get
+        // their dx and dw terms.  The ring holds the two current rows and
+        // D - 1 rows ahead.
+        for (int64_t it = 0; it < iters; it += 2) {
+            issue(it + D - 1);
+            issue(it + D);
+            cp_async_wait<D - 1>();          // this thread's copies of rows it, it+1 landed
+            float h[2], l[2];
+            row_dot(it, h[0], l[0]);
+            row_dot(it + 1, h[1], l[1]);
+            group_sum_two<kBwdMaxThreads>(h, l, red_h, red_l, tot_h, tot_l, grp, tpr);
+            row_dx(it, h[0], l[0]);
+            row_dx(it + 1, h[1], l[1]);
+            if ((it + 2) % kDwBlock == 0) fold();
+        }
+    } else {
+        for (int64_t it = 0; it < iters; ++it) {
+            issue(it + D);                   // keep D rows ahead in flight
+            cp_async_wait<D>();              // this thread's copies of row `it` landed
+            float h, l;
+            row_dot(it, h, l);
+            if constexpr (SUB)
+                pair_reduce_lanes(h, l, tpr);
+            else
+                group_sum_pair(h, l, red_h, red_l, tot_h, tot_l, grp, tpr);
+            row_dx(it, h, l);
+            if ((it + 1) % kDwBlock == 0) fold();
+        }
     }
     fold();
     cp_async_wait<0>();
@@ -316,7 +363,7 @@ k_rmsnorm_bwd(const BwdParams p)
 inline size_t bwd_smem_bytes(bool gres, int vec, int vpt, int threads, int rpc, int H, int D)
 {
     return (size_t)(D + 1) * bwd_stage_bytes(gres ? 3 : 2, vpt, vec, threads) +
-           ((size_t)H + (size_t)(rpc - 1) * H * 2) * sizeof(float);
+           ((size_t)vpt * (threads / rpc) * vec + (size_t)(rpc - 1) * H * 2) * sizeof(float);
 }
 
 // Launch of one instantiation: picks the chunk count from the occupancy of
