@@ -80,11 +80,10 @@ __device__ __forceinline__ void ld_smem_f2(const float *p, F2 (&f)[VEC / 2])
     }
 }
 
-// Bytes of one ring stage: NT tensors x VPT vectors per thread, plus one
-// private rstd slot per thread.
+// Bytes of one ring stage: NT tensors x VPT vectors per thread.
 __host__ __device__ constexpr int bwd_stage_bytes(int nt, int vpt, int vec, int threads)
 {
-    return nt * vpt * threads * vec * 2 + threads * 4;
+    return nt * vpt * threads * vec * 2;
 }
 
 template <bool W32, bool GRES, int VEC, int VPT, bool SUB, int D>
@@ -95,7 +94,12 @@ k_rmsnorm_bwd(const BwdParams p)
     constexpr int NT = GRES ? 3 : 2;
     constexpr int S = D + 1;                  // ring stages
     constexpr int VB = VEC * 2;               // bytes per vector
-    __shared__ float red_h[2 * kBwdMaxThreads], red_l[2 * kBwdMaxThreads], tot_h[64], tot_l[64];
+    // Multi-warp groups with a ring run the software-pipelined loop.
+    constexpr bool PIPE = !SUB && D >= 1;
+    __shared__ float red_h[PIPE ? 1 : kBwdMaxThreads], red_l[PIPE ? 1 : kBwdMaxThreads];
+    __shared__ float tot_h[32], tot_l[32];
+    // Per-warp row sums of the pipelined path: [row parity][group][warp].
+    __shared__ __align__(16) float wsum[PIPE ? 2 * kBwdMaxGroups * kBwdMaxGroupWarps : 4];
     extern __shared__ __align__(16) unsigned char dyn_smem[];
 
     const int nthr = blockDim.x;
@@ -109,23 +113,37 @@ k_rmsnorm_bwd(const BwdParams p)
     const int64_t iters = (r1 - r0 + rpc - 1) / rpc;
 
     // Shared memory: ring [S][stage], then w_eff [VPT*tpr*VEC] (zero past H),
-    // then the row-group combine area [rpc-1][H][2].
+    // then the row-group combine area [rpc-1][H][2].  w_eff is stored in two
+    // planes of four values per vector (one plane for VEC == 2), so that the
+    // 16-byte loads of a warp touch consecutive addresses.
     const int stage_bytes = bwd_stage_bytes(NT, VPT, VEC, nthr);
     unsigned char *ring = dyn_smem;
     float *wsm = reinterpret_cast<float *>(dyn_smem + (size_t)S * stage_bytes);
     float *comb = wsm + VPT * tpr * VEC;
+    const int wplane = VPT * tpr * 4;
 
     auto slot = [&](int stage, int tensor, int k) -> unsigned char * {
         return ring + (size_t)stage * stage_bytes + ((size_t)(tensor * VPT + k) * nthr + threadIdx.x) * VB;
     };
-    auto rslot = [&](int stage) -> float * {
-        return reinterpret_cast<float *>(ring + (size_t)stage * stage_bytes +
-                                         (size_t)NT * VPT * nthr * VB) + threadIdx.x;
+    auto w_at = [&](int v, int i) -> float * {
+        if constexpr (VEC == 8) return wsm + (i < 4 ? 0 : wplane) + v * 4 + (i & 3);
+        else return wsm + v * VEC + i;
+    };
+    auto ld_w = [&](int k, F2 (&we)[NW]) {
+        const int v = k * tpr + lane;
+        if constexpr (VEC == 8) {
+            const float4 a = *reinterpret_cast<const float4 *>(wsm + v * 4);
+            const float4 b = *reinterpret_cast<const float4 *>(wsm + wplane + v * 4);
+            we[0] = f2(a.x, a.y); we[1] = f2(a.z, a.w); we[2] = f2(b.x, b.y); we[3] = f2(b.z, b.w);
+        } else {
+            const float2 a = *reinterpret_cast<const float2 *>(wsm + v * VEC);
+            we[0] = f2(a.x, a.y);
+        }
     };
     // Issue the copies of iteration `it` (row r0 + grp + it*rpc) into its stage.
     auto issue = [&](int64_t it) {
         const int64_t t = r0 + grp + it * rpc;
-        if (it < iters && t < r1) {
+        if (t < r1) {
             const int stage = (int)(it % S);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
@@ -143,17 +161,13 @@ k_rmsnorm_bwd(const BwdParams p)
                     }
                 }
             }
-            cp_async_4(rslot(stage), p.rstd + t);
         }
         cp_async_commit();   // one group per iteration, empty or not
     };
 
-    // Prologue: the first rows go in flight while the weight is prepared
-    // (D rows; D - 1 when multi-warp groups take their rows in pairs).
-    constexpr bool PAIR = !SUB && D >= 1;
-    constexpr int PRO = PAIR ? D - 1 : D;
+    // Prologue: the first D rows go in flight while the weight is prepared.
 #pragma unroll
-    for (int i = 0; i < PRO; ++i) issue(i);
+    for (int i = 0; i < D; ++i) issue(i);
 
     // Effective weight f32(w + bias) of this thread's columns, in shared
     // memory; group 0 writes it, the other groups read it after a barrier.
@@ -177,24 +191,47 @@ k_rmsnorm_bwd(const BwdParams p)
                 }
             if (grp == 0)
 #pragma unroll
-                for (int i = 0; i < VEC; ++i) wsm[c + i] = 0.f;
+                for (int i = 0; i < VEC; ++i) *w_at(v, i) = 0.f;
         } else if (grp == 0) {
             if constexpr (W32) {
                 float f[VEC];
                 ld_f32_keep<VEC>(static_cast<const float *>(p.w) + c, f);
 #pragma unroll
-                for (int i = 0; i < VEC; ++i) wsm[c + i] = __fadd_rn(f[i], p.bias);
+                for (int i = 0; i < VEC; ++i) *w_at(v, i) = __fadd_rn(f[i], p.bias);
             } else {
                 BVec<VEC> wb = ld_keep<VEC>(static_cast<const uint16_t *>(p.w) + c);
 #pragma unroll
                 for (int i = 0; i < NW; ++i) {
-                    wsm[c + 2 * i] = __fadd_rn(bf_lo(wb.w[i]), p.bias);
-                    wsm[c + 2 * i + 1] = __fadd_rn(bf_hi(wb.w[i]), p.bias);
+                    *w_at(v, 2 * i) = __fadd_rn(bf_lo(wb.w[i]), p.bias);
+                    *w_at(v, 2 * i + 1) = __fadd_rn(bf_hi(wb.w[i]), p.bias);
                 }
             }
         }
     }
     if (rpc > 1) __syncthreads();
+
+    // rstd of the group's rows, BL rows at a time: lane j of each block holds
+    // the rstd of the block's j-th row (one load per lane, issued a whole
+    // block ahead) and the row's value is broadcast with a shuffle.  BL is
+    // the group width within a warp (tpr, a power of two, for sub-warp
+    // groups; 32 otherwise).
+    const int BL = tpr < 32 ? tpr : 32;
+    const int bl = lane & (BL - 1);
+    auto rs_block = [&](int64_t it0) -> float {
+        const int64_t t = r0 + grp + (it0 + bl) * rpc;
+        return t < r1 ? __ldg(p.rstd + t) : 0.f;
+    };
+    float rs_cur = rs_block(0), rs_nxt = rs_block(BL);
+    // Called by every lane of the warp together.
+    auto rs_of = [&](int64_t it) -> float {
+        return __shfl_sync(0xffffffffu, rs_cur, (int)(it & (BL - 1)), BL);
+    };
+    auto rs_advance = [&](int64_t it) {
+        if (((it + 1) & (BL - 1)) == 0) {
+            rs_cur = rs_nxt;
+            rs_nxt = rs_block(it + 1 + BL);
+        }
+    };
 
     float acc[VPT][VEC], cmp[VPT][VEC];
     F2 blk[VPT][NW];
@@ -222,92 +259,149 @@ k_rmsnorm_bwd(const BwdParams p)
             for (int i = 0; i < NW; ++i) blk[k][i] = f2(0.f);
     };
 
-    // Row sum of g*w*x over this thread's columns of iteration i's row: FP32
-    // in two lanes, then one TwoSum; zero for an iteration past the chunk.
-    auto row_dot = [&](int64_t i, float &dh, float &dl) {
-        dh = 0.f;
-        dl = 0.f;
-        if (r0 + grp + i * rpc < r1) {
-            const int stage = (int)(i % S);
+    // Vector k of a row: dot2 += g*w*x (two FP32 lanes).
+    auto dot_vec = [&](int stage, int k, const F2 (&we)[NW], F2 &dot2) {
+        const BVec<VEC> gv = ld_smem_vec<VEC>(slot(stage, 0, k));
+        const BVec<VEC> xv = ld_smem_vec<VEC>(slot(stage, 1, k));
+#pragma unroll
+        for (int e = 0; e < NW; ++e)
+            dot2 = f2_fma(f2_mul(f2_bf16(gv.w[e]), we[e]), f2_bf16(xv.w[e]), dot2);
+    };
+    // Vector k of row t: dx = rstd*(g*w) - x*(rstd^3*m) (+ g_residual), and
+    // the dw terms g*x*rstd (g*x is exact in FP32) into the block sums.
+    auto dx_vec = [&](int64_t t, int stage, int k, const F2 (&we)[NW], F2 rs2, F2 nc3) {
+        const int v = k * tpr + lane;
+        const BVec<VEC> gv = ld_smem_vec<VEC>(slot(stage, 0, k));
+        const BVec<VEC> xv = ld_smem_vec<VEC>(slot(stage, 1, k));
+        BVec<VEC> rv;
+        if constexpr (GRES) rv = ld_smem_vec<VEC>(slot(stage, 2, k));
+        BVec<VEC> o;
+#pragma unroll
+        for (int e = 0; e < NW; ++e) {
+            const F2 g2 = f2_bf16(gv.w[e]);
+            const F2 x2 = f2_bf16(xv.w[e]);
+            F2 d2 = f2_fma(x2, nc3, f2_mul(rs2, f2_mul(g2, we[e])));
+            if constexpr (GRES) d2 = f2_add(d2, f2_bf16(rv.w[e]));
+            o.w[e] = bf16_f2(d2);
+            blk[k][e] = f2_fma(f2_mul(g2, x2), rs2, blk[k][e]);
+        }
+        if (v < nvec) st_stream<VEC>(p.dx + t * p.lddx + (int64_t)v * VEC, o);
+    };
+    // rstd*1 and -rstd^3*m for a row with rstd rs and sum of g*w*x `sum`.
+    auto coefs = [&](float rs, float sum, F2 &rs2, F2 &nc3) {
+        const float m = __fdiv_rn(sum, (float)p.H);
+        rs2 = f2(rs);
+        nc3 = f2(-__fmul_rn(__fmul_rn(__fmul_rn(rs, rs), rs), m));
+    };
+
+    if constexpr (PIPE) {
+        // Multi-warp groups, software-pipelined.  Iteration `it` forms row
+        // it+1's sum of g*w*x and adds it up inside each warp (butterfly:
+        // every lane ends with the same bits) while it writes row it's dx,
+        // reading each weight vector once for both rows; one CTA barrier per
+        // row publishes the per-warp sums, and every thread then adds its
+        // group's warp sums itself in a fixed pairwise order.  Plain FP32
+        // sums (m only scales the small second term of dx).  The ring holds
+        // rows it and it+1 plus D - 1 rows ahead.
+        const int wg = lane >> 5;
+        for (int i = threadIdx.x; i < 2 * kBwdMaxGroups * kBwdMaxGroupWarps; i += nthr)
+            if (i % kBwdMaxGroupWarps >= (tpr >> 5)) wsum[i] = 0.f;   // never-written warp slots
+        auto publish = [&](int64_t i, F2 d2) {
+            float sum = __fadd_rn(f2_lo(d2), f2_hi(d2));
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, o));
+            if ((lane & 31) == 0) wsum[((int)(i & 1) * kBwdMaxGroups + grp) * kBwdMaxGroupWarps + wg] = sum;
+        };
+        auto group_total = [&](int64_t i) -> float {
+            const float4 *q = reinterpret_cast<const float4 *>(
+                wsum + ((int)(i & 1) * kBwdMaxGroups + grp) * kBwdMaxGroupWarps);
+            float v[kBwdMaxGroupWarps];
+#pragma unroll
+            for (int j = 0; j < kBwdMaxGroupWarps / 4; ++j) {
+                const float4 f = q[j];
+                v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
+            }
+#pragma unroll
+            for (int w = 1; w < kBwdMaxGroupWarps; w <<= 1)
+#pragma unroll
+                for (int j = 0; j + w < kBwdMaxGroupWarps; j += 2 * w) v[j] = __fadd_rn(v[j], v[j + w]);
+            return v[0];
+        };
+
+        cp_async_wait<D - 1>();              // row 0 landed
+        {
+            F2 dot2 = f2(0.f);
+            if (r0 + grp < r1) {
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    F2 we[NW];
+                    ld_w(k, we);
+                    dot_vec(0, k, we, dot2);
+                }
+            }
+            publish(0, dot2);
+        }
+        __syncthreads();
+        float tot = group_total(0);
+        for (int64_t it = 0; it < iters; ++it) {
+            issue(it + D);
+            cp_async_wait<D - 1>();          // this thread's copies of rows it, it+1 landed
+            const float rs = rs_of(it);
+            const int64_t t = r0 + grp + it * rpc;
+            const bool live = t < r1;
+            const bool live_n = t + rpc < r1;
+            const int st = (int)(it % S), st_n = (int)((it + 1) % S);
+            F2 rs2, nc3;
+            coefs(rs, tot, rs2, nc3);
             F2 dot2 = f2(0.f);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                const BVec<VEC> gv = ld_smem_vec<VEC>(slot(stage, 0, k));
-                const BVec<VEC> xv = ld_smem_vec<VEC>(slot(stage, 1, k));
                 F2 we[NW];
-                ld_smem_f2<VEC>(wsm + (k * tpr + lane) * VEC, we);
-#pragma unroll
-                for (int e = 0; e < NW; ++e)
-                    dot2 = f2_fma(f2_mul(f2_bf16(gv.w[e]), we[e]), f2_bf16(xv.w[e]), dot2);
+                ld_w(k, we);
+                if (live_n) dot_vec(st_n, k, we, dot2);
+                if (live) dx_vec(t, st, k, we, rs2, nc3);
             }
-            two_sum(f2_lo(dot2), f2_hi(dot2), dh, dl);
-        }
-    };
-    // dx of iteration i's row and its dw terms, given the row's compensated
-    // sum (sh, sl) of g*w*x.
-    auto row_dx = [&](int64_t i, float sh, float sl) {
-        const int64_t t = r0 + grp + i * rpc;
-        if (t >= r1) return;
-        const int stage = (int)(i % S);
-        const float rs = *rslot(stage);
-        const float m = __fdiv_rn(__fadd_rn(sh, sl), (float)p.H);
-        const F2 rs2 = f2(rs);
-        const F2 nc3 = f2(-__fmul_rn(__fmul_rn(__fmul_rn(rs, rs), rs), m));
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int v = k * tpr + lane;
-            const BVec<VEC> gv = ld_smem_vec<VEC>(slot(stage, 0, k));
-            const BVec<VEC> xv = ld_smem_vec<VEC>(slot(stage, 1, k));
-            BVec<VEC> rv;
-            if constexpr (GRES) rv = ld_smem_vec<VEC>(slot(stage, 2, k));
-            F2 we[NW];
-            ld_smem_f2<VEC>(wsm + v * VEC, we);
-            BVec<VEC> o;
-#pragma unroll
-            for (int e = 0; e < NW; ++e) {
-                const F2 g2 = f2_bf16(gv.w[e]);
-                const F2 x2 = f2_bf16(xv.w[e]);
-                // dx = rstd*(g*w) - x*(rstd^3*m) (+ g_residual)
-                F2 d2 = f2_fma(x2, nc3, f2_mul(rs2, f2_mul(g2, we[e])));
-                if constexpr (GRES) d2 = f2_add(d2, f2_bf16(rv.w[e]));
-                o.w[e] = bf16_f2(d2);
-                // dw term g*x*rstd (g*x is exact in FP32) into the block sum.
-                blk[k][e] = f2_fma(f2_mul(g2, x2), rs2, blk[k][e]);
-            }
-            if (v < nvec) st_stream<VEC>(p.dx + t * p.lddx + (int64_t)v * VEC, o);
-        }
-    };
-
-    if constexpr (PAIR) {
-        // Multi-warp groups take their rows two at a time: both rows' partial
-        // sums are formed, two warps reduce the two rows at once (half the
-        // barriers and the reduction latency per row), then both rows get
-        // their dx and dw terms.  The ring holds the two current rows and
-        // D - 1 rows ahead.
-        for (int64_t it = 0; it < iters; it += 2) {
-            issue(it + D - 1);
-            issue(it + D);
-            cp_async_wait<D - 1>();          // this thread's copies of rows it, it+1 landed
-            float h[2], l[2];
-            row_dot(it, h[0], l[0]);
-            row_dot(it + 1, h[1], l[1]);
-            group_sum_two<kBwdMaxThreads>(h, l, red_h, red_l, tot_h, tot_l, grp, tpr);
-            row_dx(it, h[0], l[0]);
-            row_dx(it + 1, h[1], l[1]);
-            if ((it + 2) % kDwBlock == 0) fold();
+            publish(it + 1, dot2);
+            if ((it + 1) % kDwBlock == 0) fold();
+            rs_advance(it);
+            __syncthreads();
+            tot = group_total(it + 1);
         }
     } else {
         for (int64_t it = 0; it < iters; ++it) {
             issue(it + D);                   // keep D rows ahead in flight
             cp_async_wait<D>();              // this thread's copies of row `it` landed
+            const float rs = rs_of(it);
+            const int64_t t = r0 + grp + it * rpc;
+            const bool live = t < r1;
+            const int st = (int)(it % S);
+            F2 dot2 = f2(0.f);
+            if (live) {
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    F2 we[NW];
+                    ld_w(k, we);
+                    dot_vec(st, k, we, dot2);
+                }
+            }
             float h, l;
-            row_dot(it, h, l);
+            two_sum(f2_lo(dot2), f2_hi(dot2), h, l);
             if constexpr (SUB)
                 pair_reduce_lanes(h, l, tpr);
             else
                 group_sum_pair(h, l, red_h, red_l, tot_h, tot_l, grp, tpr);
-            row_dx(it, h, l);
+            if (live) {
+                F2 rs2, nc3;
+                coefs(rs, __fadd_rn(h, l), rs2, nc3);
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    F2 we[NW];
+                    ld_w(k, we);
+                    dx_vec(t, st, k, we, rs2, nc3);
+                }
+            }
             if ((it + 1) % kDwBlock == 0) fold();
+            rs_advance(it);
         }
     }
     fold();

@@ -57,14 +57,14 @@ __device__ __forceinline__ F2 f2(float lo, float hi)
 __device__ __forceinline__ F2 f2(float a) { return f2(a, a); }
 __device__ __forceinline__ float f2_lo(F2 a)
 {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+    float lo;
+    asm("mov.b64 {%0, _}, %1;" : "=f"(lo) : "l"(a.v));
     return lo;
 }
 __device__ __forceinline__ float f2_hi(F2 a)
 {
-    float lo, hi;
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+    float hi;
+    asm("mov.b64 {_, %0}, %1;" : "=f"(hi) : "l"(a.v));
     return hi;
 }
 __device__ __forceinline__ F2 f2_add(F2 a, F2 b)
@@ -256,62 +256,6 @@ __device__ __forceinline__ void group_sum_pair(float &h, float &l, float *red_h,
     __syncthreads();
     h = tot_h[grp];
     l = tot_l[grp];
-}
-
-// Sums of the pairs of two rows (index 0 and 1) over the tpr threads of each
-// multi-warp row group (tpr >= 64), returned to every thread of the group.
-// Every thread stores its two pairs; warp r of the group adds row r's pairs:
-// lane i loads the pairs of threads i, i+32, ... and adds them in a fixed
-// pairwise tree, then the 32 lane sums meet in a butterfly.  The two rows
-// are reduced at the same time by two warps.  red_h / red_l hold 2 x MAXT
-// slots, tot_h / tot_l 2 x 32 (one per group and row).  Two CTA barriers.
-template <int MAXT>
-__device__ __forceinline__ void group_sum_two(float (&h)[2], float (&l)[2], float *red_h,
-                                              float *red_l, float *tot_h, float *tot_l, int grp,
-                                              int tpr)
-{
-    constexpr int NJ = MAXT / 32;
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        red_h[r * MAXT + threadIdx.x] = h[r];
-        red_l[r * MAXT + threadIdx.x] = l[r];
-    }
-    __syncthreads();
-    const int base = grp * tpr;
-    const int wi = (threadIdx.x - base) >> 5;
-    const int lane32 = threadIdx.x & 31;
-    if (wi < 2) {
-        const float *rh = red_h + wi * MAXT + base;
-        const float *rl = red_l + wi * MAXT + base;
-        float hv[NJ], lv[NJ];
-#pragma unroll
-        for (int j = 0; j < NJ; ++j) {
-            const int src = lane32 + 32 * j;
-            hv[j] = src < tpr ? rh[src] : 0.f;
-            lv[j] = src < tpr ? rl[src] : 0.f;
-        }
-#pragma unroll
-        for (int w = 1; w < NJ; w <<= 1)
-#pragma unroll
-            for (int j = 0; j + w < NJ; j += 2 * w) pair_acc(hv[j], lv[j], hv[j + w], lv[j + w]);
-        float th = hv[0], tl = lv[0];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float bh = __shfl_xor_sync(0xffffffffu, th, o);
-            const float bl = __shfl_xor_sync(0xffffffffu, tl, o);
-            pair_acc(th, tl, bh, bl);
-        }
-        if (lane32 == 0) {
-            tot_h[wi * 32 + grp] = th;
-            tot_l[wi * 32 + grp] = tl;
-        }
-    }
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        h[r] = tot_h[r * 32 + grp];
-        l[r] = tot_l[r * 32 + grp];
-    }
 }
 
 }  // namespace crmsn

@@ -15,6 +15,11 @@ constexpr int kFwdMaxThreads = 512;
 constexpr int kBwdMaxThreads = 512;
 // The backward workspace holds at most this many partial rows per SM.
 constexpr int kBwdMaxCtasPerSm = 2;
+// Multi-warp row groups of the backward: at most this many per CTA (a group
+// has at least 96 threads and a CTA at most 256 threads' worth of groups)
+// and at most this many warps each.
+constexpr int kBwdMaxGroups = 4;
+constexpr int kBwdMaxGroupWarps = kBwdMaxThreads / 32;
 
 enum InKind { IN_PLAIN = 0, IN_RESIDUAL = 1, IN_GATED = 2 };
 enum OutKind {
