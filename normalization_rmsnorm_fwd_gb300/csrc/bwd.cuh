@@ -80,6 +80,19 @@ __device__ __forceinline__ void ld_smem_f2(const float *p, F2 (&f)[VEC / 2])
     }
 }
 
+// Exact FP32 products of the two BF16 pairs packed in g and x (low halves,
+// high halves): one mixed-precision FMA (BF16 operands, FP32 addend and
+// result, sm_100 and later) per product, no unpacking.  A product of two
+// BF16 values has at most 16 significant bits, so it is exact in FP32.
+__device__ __forceinline__ F2 mul_bf16x2(uint32_t g, uint32_t x)
+{
+    float lo, hi;
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %2;\n\tmov.b32 {b0, b1}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, a0, b0, %4;\n\tfma.rn.f32.bf16 %1, a1, b1, %4;\n}"
+        : "=f"(lo), "=f"(hi) : "r"(g), "r"(x), "f"(0.f));
+    return f2(lo, hi);
+}
+
 // Bytes of one ring stage: NT tensors x VPT vectors per thread.
 __host__ __device__ constexpr int bwd_stage_bytes(int nt, int vpt, int vec, int threads)
 {
@@ -214,7 +227,8 @@ k_rmsnorm_bwd(const BwdParams p)
     // the rstd of the block's j-th row (one load per lane, issued a whole
     // block ahead) and the row's value is broadcast with a shuffle.  BL is
     // the group width within a warp (tpr, a power of two, for sub-warp
-    // groups; 32 otherwise).
+    // groups; 32 otherwise).  rs_cur holds the block of the current
+    // iteration, rs_nxt the next block.
     const int BL = tpr < 32 ? tpr : 32;
     const int bl = lane & (BL - 1);
     auto rs_block = [&](int64_t it0) -> float {
@@ -222,9 +236,11 @@ k_rmsnorm_bwd(const BwdParams p)
         return t < r1 ? __ldg(p.rstd + t) : 0.f;
     };
     float rs_cur = rs_block(0), rs_nxt = rs_block(BL);
-    // Called by every lane of the warp together.
-    auto rs_of = [&](int64_t it) -> float {
-        return __shfl_sync(0xffffffffu, rs_cur, (int)(it & (BL - 1)), BL);
+    // rstd of iteration i, i in the current (it's) or the next block; called
+    // by every lane of the warp together.
+    auto rs_of = [&](int64_t i, int64_t it) -> float {
+        const float src = ((i ^ it) & ~(int64_t)(BL - 1)) == 0 ? rs_cur : rs_nxt;
+        return __shfl_sync(0xffffffffu, src, (int)(i & (BL - 1)), BL);
     };
     auto rs_advance = [&](int64_t it) {
         if (((it + 1) & (BL - 1)) == 0) {
@@ -267,9 +283,22 @@ k_rmsnorm_bwd(const BwdParams p)
         for (int e = 0; e < NW; ++e)
             dot2 = f2_fma(f2_mul(f2_bf16(gv.w[e]), we[e]), f2_bf16(xv.w[e]), dot2);
     };
+    // Vector k of a row with rstd rs2: dot2 += (g*x)*w, and the dw terms
+    // (g*x)*rstd into the block sums, from the exact products g*x.
+    auto dot_dw_vec = [&](int stage, int k, const F2 (&we)[NW], F2 rs2, F2 &dot2) {
+        const BVec<VEC> gv = ld_smem_vec<VEC>(slot(stage, 0, k));
+        const BVec<VEC> xv = ld_smem_vec<VEC>(slot(stage, 1, k));
+#pragma unroll
+        for (int e = 0; e < NW; ++e) {
+            const F2 gx = mul_bf16x2(gv.w[e], xv.w[e]);
+            dot2 = f2_fma(gx, we[e], dot2);
+            blk[k][e] = f2_fma(gx, rs2, blk[k][e]);
+        }
+    };
     // Vector k of row t: dx = rstd*(g*w) - x*(rstd^3*m) (+ g_residual), and
-    // the dw terms g*x*rstd (g*x is exact in FP32) into the block sums.
-    auto dx_vec = [&](int64_t t, int stage, int k, const F2 (&we)[NW], F2 rs2, F2 nc3) {
+    // with with_dw the dw terms g*x*rstd (g*x is exact in FP32) into the block
+    // sums.
+    auto dx_vec = [&](bool with_dw, int64_t t, int stage, int k, const F2 (&we)[NW], F2 rs2, F2 nc3) {
         const int v = k * tpr + lane;
         const BVec<VEC> gv = ld_smem_vec<VEC>(slot(stage, 0, k));
         const BVec<VEC> xv = ld_smem_vec<VEC>(slot(stage, 1, k));
@@ -283,7 +312,7 @@ k_rmsnorm_bwd(const BwdParams p)
             F2 d2 = f2_fma(x2, nc3, f2_mul(rs2, f2_mul(g2, we[e])));
             if constexpr (GRES) d2 = f2_add(d2, f2_bf16(rv.w[e]));
             o.w[e] = bf16_f2(d2);
-            blk[k][e] = f2_fma(f2_mul(g2, x2), rs2, blk[k][e]);
+            if (with_dw) blk[k][e] = f2_fma(f2_mul(g2, x2), rs2, blk[k][e]);
         }
         if (v < nvec) st_stream<VEC>(p.dx + t * p.lddx + (int64_t)v * VEC, o);
     };
@@ -328,15 +357,18 @@ k_rmsnorm_bwd(const BwdParams p)
             return v[0];
         };
 
+        // The dw terms of a row are taken in its sum phase, from the exact
+        // products g*x; block sums fold after every kDwBlock rows as before.
         cp_async_wait<D - 1>();              // row 0 landed
         {
+            const F2 rs2 = f2(rs_of(0, 0));
             F2 dot2 = f2(0.f);
             if (r0 + grp < r1) {
 #pragma unroll
                 for (int k = 0; k < VPT; ++k) {
                     F2 we[NW];
                     ld_w(k, we);
-                    dot_vec(0, k, we, dot2);
+                    dot_dw_vec(0, k, we, rs2, dot2);
                 }
             }
             publish(0, dot2);
@@ -346,7 +378,8 @@ k_rmsnorm_bwd(const BwdParams p)
         for (int64_t it = 0; it < iters; ++it) {
             issue(it + D);
             cp_async_wait<D - 1>();          // this thread's copies of rows it, it+1 landed
-            const float rs = rs_of(it);
+            const float rs = rs_of(it, it);
+            const F2 rsn2 = f2(rs_of(it + 1, it));
             const int64_t t = r0 + grp + it * rpc;
             const bool live = t < r1;
             const bool live_n = t + rpc < r1;
@@ -358,11 +391,11 @@ k_rmsnorm_bwd(const BwdParams p)
             for (int k = 0; k < VPT; ++k) {
                 F2 we[NW];
                 ld_w(k, we);
-                if (live_n) dot_vec(st_n, k, we, dot2);
-                if (live) dx_vec(t, st, k, we, rs2, nc3);
+                if (live_n) dot_dw_vec(st_n, k, we, rsn2, dot2);
+                if (live) dx_vec(false, t, st, k, we, rs2, nc3);
             }
             publish(it + 1, dot2);
-            if ((it + 1) % kDwBlock == 0) fold();
+            if ((it + 2) % kDwBlock == 0) fold();
             rs_advance(it);
             __syncthreads();
             tot = group_total(it + 1);
@@ -371,7 +404,7 @@ k_rmsnorm_bwd(const BwdParams p)
         for (int64_t it = 0; it < iters; ++it) {
             issue(it + D);                   // keep D rows ahead in flight
             cp_async_wait<D>();              // this thread's copies of row `it` landed
-            const float rs = rs_of(it);
+            const float rs = rs_of(it, it);
             const int64_t t = r0 + grp + it * rpc;
             const bool live = t < r1;
             const int st = (int)(it % S);
@@ -397,7 +430,7 @@ k_rmsnorm_bwd(const BwdParams p)
                 for (int k = 0; k < VPT; ++k) {
                     F2 we[NW];
                     ld_w(k, we);
-                    dx_vec(t, st, k, we, rs2, nc3);
+                    dx_vec(true, t, st, k, we, rs2, nc3);
                 }
             }
             if ((it + 1) % kDwBlock == 0) fold();
