@@ -5,18 +5,22 @@
 
 namespace crmsn {
 
-// dw[j] = sum over chunks c (in order) of part[c][j], compensated.  A block
-// covers 32 consecutive columns, one per lane; its warps each sum a fixed
-// contiguous range of chunks, issuing the loads of up to kBatch chunks
-// before adding them, and warp 0 adds the warps' pair sums in warp order.
-constexpr int kReduceWarps = 16;
-constexpr int kBatch = 8;
+// dw[j] = sum over chunks c of part[c][j], compensated, in a fixed order.
+// A block covers 32 consecutive columns, one per lane, with kReduceWarps
+// warps; warp w sums the contiguous chunk range [w*n/W, (w+1)*n/W) in chunk
+// order, issuing all its loads (up to kBatch at a time) before adding them.
+// The warps' pairs then meet in a fixed butterfly: warp j takes column j,
+// lane i holding warp i's pair.  One round trip to L2 (where the partials
+// were just written) for up to kBatch*kReduceWarps chunks, and no serial
+// combine.
+constexpr int kReduceWarps = 32;
+constexpr int kBatch = 16;
 
 __global__ void __launch_bounds__(32 * kReduceWarps)
 k_dw_reduce(const float *__restrict__ part, int nchunk, int H, float *__restrict__ dw)
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    __shared__ float sh_h[kReduceWarps][32], sh_l[kReduceWarps][32];
+    __shared__ float sh_h[kReduceWarps][33], sh_l[kReduceWarps][33];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
     const int col = blockIdx.x * 32 + lane;
@@ -41,11 +45,11 @@ k_dw_reduce(const float *__restrict__ part, int nchunk, int H, float *__restrict
     sh_h[warp][lane] = h;
     sh_l[warp][lane] = l;
     __syncthreads();
-    if (warp == 0 && col < H) {
-        float a = sh_h[0][lane], b = sh_l[0][lane];
-        for (int w = 1; w < kReduceWarps; ++w) pair_add(a, b, sh_h[w][lane], sh_l[w][lane]);
-        dw[col] = __fadd_rn(a, b);
-    }
+    // Warp j: column j of the block; lane i: warp i's pair.
+    float a = sh_h[lane][warp], b = sh_l[lane][warp];
+    pair_reduce_lanes(a, b, 32);
+    const int out = blockIdx.x * 32 + warp;
+    if (lane == 0 && out < H) dw[out] = __fadd_rn(a, b);
 }
 
 static cudaError_t launch_dw_reduce(const float *part, int nchunk, int H, float *dw, cudaStream_t s)

@@ -155,3 +155,17 @@ def test_dx_in_place_over_g(orc):
     ref = orc.rmsnorm_bwd(g, x, w, rstd)
     allow = gu.dx_allowance(g, x, orc.weight_eff(w), rstd, ref["m"])
     gu.check_bf16(gu.host_bits(gd), ref["dx_exact"], allowance=allow, what="dx in place")
+
+
+@pytest.mark.parametrize("H", [1024, 4096])
+@pytest.mark.parametrize("T", [305, 608, 913, 1500, 2431])
+def test_pipelined_chunk_lengths(orc, H, T):
+    # Multi-warp rows run the software-pipelined loop (row i+1's sum formed
+    # while row i's dx is written); these row counts give chunks of one to
+    # eight rows, so the prologue, the steady state and the tail (rows past
+    # the chunk) all occur, with one and two row groups per CTA (H = 4096 and
+    # H = 1024).
+    g, x = synth.random_rows(T + H, T, H, n=2)
+    w = synth.random_weight(T + 7, H)
+    compare(orc, g, x, w, rows=None if T < 1000 else gu.sample_rows(T))
+
