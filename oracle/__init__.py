@@ -92,6 +92,10 @@ _SIGS = {
     "orc_ada_rms_norm_style": (None, [_I, _I, _P, _P, _P, _I, _F, _P, _P, _P]),
     "orc_gate_residual_ada_norm_fp8": (None, [_I, _I, _P, _P, _P, _P, _P, _I,
                                               _F, _F, _P, _P, _P, _P]),
+    "orc_fused_rmsnorm_silu": (None, [_I, _I, _P, _I, _P, _INT, _F, _F, _INT, _F,
+                                      _P, _P, _P, _P]),
+    "orc_layernorm": (None, [_I, _I, _P, _I, _P, _P, _F, _INT, _INT, _F, _P, _P,
+                             _P, _P, _P]),
 }
 
 
@@ -299,6 +303,35 @@ class Oracle:
             float(scale), float(eps), _ptr(residual_out), _ptr(v_exact), _ptr(q), _ptr(gate_out))
         return dict(residual_out=residual_out, v_exact=v_exact, q=q, gate_out=gate_out)
 
+
+    def fused_rmsnorm_silu(self, x, w, eps, weight_bias=0.0, fp8=False, scale=1.0):
+        x, ldx = _rows(x, np.uint16)
+        T, H = x.shape
+        w, is32 = _weight(w)
+        v_exact = np.empty((T, H), np.float64)
+        y = None if fp8 else np.empty((T, H), np.uint16)
+        q = np.empty((T, H), np.uint8) if fp8 else None
+        rstd32 = np.empty(T, np.float32)
+        self.L.orc_fused_rmsnorm_silu(T, H, _ptr(x), ldx, _ptr(w), is32, float(weight_bias),
+                                      float(eps), int(bool(fp8)), float(scale), _ptr(v_exact),
+                                      _ptr(y), _ptr(q), _ptr(rstd32))
+        return dict(v_exact=v_exact, y=y, q=q, rstd=rstd32)
+
+    def layernorm(self, x, gamma, beta, eps, fp8_kind=None, scale=1.0):
+        x, ldx = _rows(x, np.uint16)
+        T, H = x.shape
+        gamma = np.ascontiguousarray(gamma, np.float32)
+        beta = np.ascontiguousarray(beta, np.float32)
+        fp8 = fp8_kind is not None
+        v_exact = np.empty((T, H), np.float64)
+        y = None if fp8 else np.empty((T, H), np.uint16)
+        q = np.empty((T, H), np.uint8) if fp8 else None
+        mean = np.empty(T, np.float64)
+        rstd = np.empty(T, np.float64)
+        self.L.orc_layernorm(T, H, _ptr(x), ldx, _ptr(gamma), _ptr(beta), float(eps), int(fp8),
+                             int(fp8_kind or 0), float(scale), _ptr(v_exact), _ptr(y), _ptr(q),
+                             _ptr(mean), _ptr(rstd))
+        return dict(v_exact=v_exact, y=y, q=q, mean=mean, rstd=rstd)
 
 _default: Oracle | None = None
 

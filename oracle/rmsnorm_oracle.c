@@ -506,3 +506,95 @@ void orc_gate_residual_ada_norm_fp8(int64_t T, int64_t D,
     free(we);
     free(yv);
 }
+
+/* [API] fused_rmsnorm_silu, [GUIDE] 5.1: out = SiLU(RMSNorm(input, weight,
+ * eps)) with SiLU(v) = v / (1 + exp(-v)), applied to the unrounded
+ * normalised value yv.  BF16 output: bf16(SiLU(yv)).  FP8 output (E4M3FN):
+ * the nearest code of the FP32 value f32(SiLU(yv) / scale); the guide names
+ * no scale for this operation, so scale = 1 is the plain cast.  v_exact
+ * (nullable) receives SiLU(yv) / scale (scale 1 for the BF16 output). */
+void orc_fused_rmsnorm_silu(int64_t T, int64_t H,
+                            const uint16_t *x, int64_t ldx,
+                            const void *w, int w_is_f32, float weight_bias,
+                            float eps, int out_fp8, float scale,
+                            double *v_exact, uint16_t *y, uint8_t *q,
+                            float *rstd32)
+{
+    double *h = malloc(sizeof(double) * (size_t)H);
+    double *we = malloc(sizeof(double) * (size_t)H);
+    double *yv = malloc(sizeof(double) * (size_t)H);
+    orc_weight_eff(H, w, w_is_f32, weight_bias, we);
+    for (int64_t t = 0; t < T; ++t) {
+        load_row(t, H, x, ldx, NULL, 0, h, NULL);
+        double r = orc_row_fwd_f64(H, h, we, (double)eps, yv);
+        for (int64_t j = 0; j < H; ++j) {
+            double s = yv[j] / (1.0 + exp(-yv[j]));
+            if (out_fp8) {
+                double v = s / (double)scale;
+                if (v_exact)
+                    v_exact[t * H + j] = v;
+                q[t * H + j] = orc_e4m3_from_f32((float)v);
+            } else {
+                if (v_exact)
+                    v_exact[t * H + j] = s;
+                y[t * H + j] = orc_bf16_from_f64(s);
+            }
+        }
+        if (rstd32)
+            rstd32[t] = (float)r;
+    }
+    free(h);
+    free(we);
+    free(yv);
+}
+
+/* [API] layernorm / layernorm_quant, [GUIDE] 4: BF16 input, FP32 gamma and
+ * beta,
+ *   out = ((x - E[x]) / sqrt(Var[x] + eps)) * gamma + beta,
+ * Var the mean of the squared deviations from E[x] (divisor H: the reading
+ * of a layer's variance over its features).  BF16 output: bf16(out).
+ * layernorm_quant divides by the FP32 scale before the FP8 cast (E4M3FN or
+ * E5M2 by fp8_kind), decided on the FP32 value f32(out / scale).  v_exact
+ * (nullable) receives out (BF16) or out / scale (FP8); mean_out and
+ * rstd_out (nullable) E[x] and 1 / sqrt(Var[x] + eps) per row. */
+void orc_layernorm(int64_t T, int64_t H,
+                   const uint16_t *x, int64_t ldx,
+                   const float *gamma, const float *beta, float eps,
+                   int out_fp8, int fp8_kind, float scale,
+                   double *v_exact, uint16_t *y, uint8_t *q,
+                   double *mean_out, double *rstd_out)
+{
+    double *h = malloc(sizeof(double) * (size_t)H);
+    for (int64_t t = 0; t < T; ++t) {
+        double sum = 0.0;
+        for (int64_t j = 0; j < H; ++j) {
+            h[j] = orc_bf16_to_f64(x[t * ldx + j]);
+            sum += h[j];
+        }
+        double mean = sum / (double)H;
+        double sq = 0.0;
+        for (int64_t j = 0; j < H; ++j)
+            sq += (h[j] - mean) * (h[j] - mean);
+        double var = sq / (double)H;
+        double rstd = 1.0 / sqrt(var + (double)eps);
+        if (mean_out)
+            mean_out[t] = mean;
+        if (rstd_out)
+            rstd_out[t] = rstd;
+        for (int64_t j = 0; j < H; ++j) {
+            double o = (h[j] - mean) * rstd * (double)gamma[j] + (double)beta[j];
+            if (out_fp8) {
+                double v = o / (double)scale;
+                if (v_exact)
+                    v_exact[t * H + j] = v;
+                float v32 = (float)v;
+                q[t * H + j] = fp8_kind ? orc_e5m2_from_f32(v32) : orc_e4m3_from_f32(v32);
+            } else {
+                if (v_exact)
+                    v_exact[t * H + j] = o;
+                y[t * H + j] = orc_bf16_from_f64(o);
+            }
+        }
+    }
+    free(h);
+}

@@ -127,6 +127,27 @@ void orc_gate_residual_ada_norm_fp8(int64_t T, int64_t D,
                             uint16_t *residual_out, double *v_exact, uint8_t *q,
                             uint16_t *gate_out);
 
+/* RMSNorm + SiLU: s = yv / (1 + exp(-yv)) of the plain forward's yv.
+ * out_fp8 == 0: y = bf16(s), v_exact = s.  out_fp8 != 0: q = e4m3(f32(s /
+ * scale)), v_exact = s / scale.  y or q may be NULL for the other output. */
+void orc_fused_rmsnorm_silu(int64_t T, int64_t H,
+                            const uint16_t *x, int64_t ldx,
+                            const void *w, int w_is_f32, float weight_bias,
+                            float eps, int out_fp8, float scale,
+                            double *v_exact, uint16_t *y, uint8_t *q,
+                            float *rstd32);
+
+/* LayerNorm: o = (x - mean) * rstd * gamma + beta, rstd = 1/sqrt(var + eps),
+ * var the population variance.  out_fp8 == 0: y = bf16(o), v_exact = o.
+ * out_fp8 != 0: q = fp8(f32(o / scale)) (fp8_kind 0 E4M3FN, 1 E5M2),
+ * v_exact = o / scale.  mean_out, rstd_out, v_exact nullable. */
+void orc_layernorm(int64_t T, int64_t H,
+                   const uint16_t *x, int64_t ldx,
+                   const float *gamma, const float *beta, float eps,
+                   int out_fp8, int fp8_kind, float scale,
+                   double *v_exact, uint16_t *y, uint8_t *q,
+                   double *mean_out, double *rstd_out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -475,4 +475,85 @@ def pin_gated_ada(o):
     assert np.array_equal(zero["residual_out"], u)
 
 
+# ------------------------------------------------------------ SiLU, LayerNorm --
+
+def pin_silu(o):
+    """RMSNorm + SiLU: v is PyTorch's float64 SiLU of the forward's exact
+    value (plain, Gemma and FP32-weight routes); SiLU(v) - SiLU(-v) = v on
+    negated rows; a row [a, -a] gives SiLU(+-a*rstd) in closed form; BF16
+    outputs are the nearest BF16 and FP8 codes the nearest E4M3 of
+    f32(v / scale), saturating."""
+    T, H = 6, 160
+    x = synth.random_rows(40, T, H)[0]
+    for w, bias in ((synth.random_weight(40, H), 0.0), (synth.random_weight(41, H), 1.0),
+                    (synth.random_weight(42, H, f32=True), 1.0)):
+        r = o.fused_rmsnorm_silu(x, w, 1e-6, weight_bias=bias)
+        f = o.rmsnorm_fwd(x, w, 1e-6, weight_bias=bias)
+        ref = torch.nn.functional.silu(torch.from_numpy(f["y_exact"])).numpy()
+        _close(r["v_exact"], ref, 1e-14, "silu vs torch")
+        assert np.array_equal(r["y"], numfmt.nearest_bf16(r["v_exact"]))
+        assert np.array_equal(r["rstd"], f["rstd"])
+        neg = o.fused_rmsnorm_silu(x ^ np.uint16(0x8000), w, 1e-6, weight_bias=bias)
+        _close(r["v_exact"] - neg["v_exact"], f["y_exact"], 1e-12, "silu(v) - silu(-v) = v")
+        for scale in (1.0, 0.04):
+            qr = o.fused_rmsnorm_silu(x, w, 1e-6, weight_bias=bias, fp8=True, scale=scale)
+            _close(qr["v_exact"] * float(np.float32(scale)), r["v_exact"], 4e-16, "v * scale")
+            want = numfmt.nearest_fp8(qr["v_exact"].astype(np.float32).astype(np.float64), 0)
+            assert np.array_equal(qr["q"], want), scale
+    a = 3.0
+    row = _bits([[a, -a]])
+    r = o.fused_rmsnorm_silu(row, _bits([1.0, 1.0]), 1e-6)
+    rs = 1.0 / math.sqrt(a * a + float(np.float32(1e-6)))
+    want = [a * rs / (1.0 + math.exp(-a * rs)), -a * rs / (1.0 + math.exp(a * rs))]
+    _close(r["v_exact"][0], want, 1e-15, "silu closed form")
+
+
+def pin_layernorm(o):
+    """LayerNorm: v is PyTorch's float64 layer_norm (population variance, eps
+    inside the root) with gamma and beta; the mean and rstd are numpy's
+    mean and 1/sqrt(var + eps); shifting a row by a constant changes
+    nothing; with gamma = 1, beta = 0 a row sums to 0 and its mean square is
+    var / (var + eps); a two-element row is +-|a-b|/2 / sqrt(((a-b)/2)^2 +
+    eps) in closed form; BF16 outputs are the nearest BF16 and FP8 codes the
+    nearest E4M3 / E5M2 of f32(v / scale)."""
+    T, H = 5, 192
+    x = synth.random_rows(50, T, H)[0]
+    gen = torch.Generator().manual_seed(51)
+    gamma = (1 + 0.1 * torch.randn(H, generator=gen)).numpy().astype(np.float32)
+    beta = (0.1 * torch.randn(H, generator=gen)).numpy().astype(np.float32)
+    eps = 1e-5
+    e32 = float(np.float32(eps))
+    r = o.layernorm(x, gamma, beta, eps)
+    xd = numfmt.decode_bf16(x)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(xd), (H,),
+                                         torch.from_numpy(gamma.astype(np.float64)),
+                                         torch.from_numpy(beta.astype(np.float64)), e32).numpy()
+    _close(r["v_exact"], ref, 1e-12, "layernorm vs torch")
+    _close(r["mean"], xd.mean(axis=1), 1e-14, "mean")
+    _close(r["rstd"], 1.0 / np.sqrt(xd.var(axis=1) + e32), 1e-14, "rstd")
+    assert np.array_equal(r["y"], numfmt.nearest_bf16(r["v_exact"]))
+    one, zero = np.ones(H, np.float32), np.zeros(H, np.float32)
+    p = o.layernorm(x, one, zero, eps)
+    var = xd.var(axis=1)
+    assert np.all(np.abs(p["v_exact"].sum(axis=1)) <= 1e-12 * H)
+    _close((p["v_exact"] ** 2).mean(axis=1), var / (var + e32), 1e-13, "mean square")
+    ints = np.arange(-40, 40, dtype=np.float64).reshape(1, 80)
+    xi = numfmt.nearest_bf16(ints)
+    xs = numfmt.nearest_bf16(ints + 64.0)           # exact: integers below 256
+    a1 = o.layernorm(xi, np.ones(80, np.float32), np.zeros(80, np.float32), eps)
+    a2 = o.layernorm(xs, np.ones(80, np.float32), np.zeros(80, np.float32), eps)
+    _close(a2["v_exact"], a1["v_exact"], 1e-13, "shift invariance")
+    a, b = 5.0, 2.0
+    two = o.layernorm(_bits([[a, b]]), np.array([2.0, 3.0], np.float32),
+                      np.array([0.5, -1.0], np.float32), eps)
+    d = abs(a - b) / 2 / math.sqrt(((a - b) / 2) ** 2 + e32)
+    _close(two["v_exact"][0], [d * 2.0 + 0.5, -d * 3.0 - 1.0], 1e-15, "two-element row")
+    for kind in (0, 1):
+        for scale in (0.04, 1.0):
+            qr = o.layernorm(x, gamma, beta, eps, fp8_kind=kind, scale=scale)
+            _close(qr["v_exact"] * float(np.float32(scale)), r["v_exact"], 4e-16, "v * scale")
+            want = numfmt.nearest_fp8(qr["v_exact"].astype(np.float32).astype(np.float64), kind)
+            assert np.array_equal(qr["q"], want), (kind, scale)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -42,6 +42,14 @@ MUTANTS = [
     ("gated_product_unrounded", "double prod = orc_bf16_to_f64(orc_bf16_from_f64(xg));", "double prod = xg;", 0),
     ("gated_gate_from_shift", "gate_out[t * D + j] = st[2 * D + j];", "gate_out[t * D + j] = st[D + j];", 1),
     ("gated_no_one_plus", "double v = (yv[j] * (1.0 + sc) + sh) / (double)scale;", "double v = (yv[j] * sc + sh) / (double)scale;", 0),
+    ("silu_exp_sign", "double s = yv[j] / (1.0 + exp(-yv[j]));", "double s = yv[j] / (1.0 + exp(yv[j]));", 0),
+    ("silu_sigmoid_only", "double s = yv[j] / (1.0 + exp(-yv[j]));", "double s = 1.0 / (1.0 + exp(-yv[j]));", 0),
+    ("silu_fp8_multiplies", "double v = s / (double)scale;", "double v = s * (double)scale;", 0),
+    ("ln_unbiased_var", "double var = sq / (double)H;", "double var = sq / (double)(H - 1);", 0),
+    ("ln_beta_dropped", "* rstd * (double)gamma[j] + (double)beta[j];", "* rstd * (double)gamma[j];", 0),
+    ("ln_not_centred", "double o = (h[j] - mean) * rstd", "double o = h[j] * rstd", 0),
+    ("ln_eps_outside_root", "1.0 / sqrt(var + (double)eps)", "1.0 / (sqrt(var) + (double)eps)", 0),
+    ("ln_quant_formats_swapped", "fp8_kind ? orc_e5m2_from_f32(v32) : orc_e4m3_from_f32(v32)", "fp8_kind ? orc_e4m3_from_f32(v32) : orc_e5m2_from_f32(v32)", 1),
 ]
 
 
