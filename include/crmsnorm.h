@@ -3,8 +3,8 @@
  *
  * Row-wise RMSNorm forward (plain, fused residual add, Gemma w+1, FP32
  * zero-centred weight), its FP8 epilogues (static scale, 1x128 blocks), the
- * AdaRMSNorm style epilogues, and the training backward (dx and a
- * deterministic FP32 dw).
+ * AdaRMSNorm style epilogues, RMSNorm + SiLU, LayerNorm (BF16 and FP8
+ * output), and the training backward (dx and a deterministic FP32 dw).
  *
  * Sources cited below:
  *   [API]   "flashinfer.norm" API index (docs.flashinfer.ai/api/norm.html)
@@ -69,6 +69,8 @@ typedef enum crmsn_status {
 enum { CRMSN_BF16 = 0, CRMSN_F32 = 1 };
 /* FP8 output formats. */
 enum { CRMSN_E4M3 = 0, CRMSN_E5M2 = 1 };
+/* Output formats of fused_rmsnorm_silu. */
+enum { CRMSN_OUT_BF16 = 0, CRMSN_OUT_E4M3 = 1 };
 /* Operation ids for rmsnorm_supports(). */
 enum {
     CRMSN_OP_FWD = 0,
@@ -76,7 +78,9 @@ enum {
     CRMSN_OP_QUANT = 2,
     CRMSN_OP_BLOCK_QUANT = 3,
     CRMSN_OP_ADA_STYLE = 4,
-    CRMSN_OP_GATED_ADA_FP8 = 5
+    CRMSN_OP_GATED_ADA_FP8 = 5,
+    CRMSN_OP_SILU = 6,
+    CRMSN_OP_LAYERNORM = 7
 };
 
 /* Largest supported hidden size. */
@@ -262,6 +266,67 @@ crmsn_status gate_residual_ada_norm_fp8(void *residual, const void *x,
                                         int64_t T, int64_t D,
                                         void *out, void *gate_out,
                                         cudaStream_t stream);
+
+/*
+ * fused_rmsnorm_silu -- [API] fused_rmsnorm_silu; [GUIDE] 5.1.
+ *
+ *   v[t,j] = (x[t,j] * rstd[t]) * w_eff[j]   (the plain rmsnorm_fwd value)
+ *   s      = SiLU(v) = v / (1 + exp(-v))    (FP32; see the error note below)
+ *   CRMSN_OUT_BF16: out = bf16(s)
+ *   CRMSN_OUT_E4M3: out = e4m3(s / scale), saturating to +-448; scale is a
+ *                   device FP32 [1] or NULL for no scale (the guide names none)
+ *
+ * x: BF16 [T, H], row stride ldx.  out: BF16 or E4M3FN [T, H], row stride
+ * ldo; a BF16 out may be x itself (same pointer and stride).  w: BF16 or FP32
+ * [H] (w_dtype) with weight_bias as in rmsnorm_fwd.  rstd: FP32 [T] or NULL.
+ * SiLU uses the fast exponential and reciprocal: its relative error is about
+ * 2^-20 where |v| < 10 and stays far below a BF16 half-ulp everywhere.  The
+ * guide's NVFP4 output is not provided.  Errors: CRMSN_ERR_DTYPE for another
+ * out_format or w_dtype; the rest as rmsnorm_fwd.  1 <= H <= CRMSN_MAX_H, H
+ * even.
+ */
+crmsn_status fused_rmsnorm_silu(void *out, int64_t ldo, int out_format,
+                                const void *x, int64_t ldx,
+                                const void *w, int w_dtype, float weight_bias,
+                                const float *scale, float eps,
+                                int64_t T, int64_t H, float *rstd,
+                                cudaStream_t stream);
+
+/*
+ * layernorm -- [API] layernorm; [GUIDE] 4.
+ *
+ *   mean[t] = (1/H) sum_j x[t,j]
+ *   var[t]  = (1/H) sum_j (x[t,j] - mean[t])^2       (population variance)
+ *   rstd[t] = 1 / sqrt(var[t] + eps)
+ *   y[t,j]  = bf16((x[t,j] - mean[t]) * rstd[t] * gamma[j] + beta[j])
+ *
+ * x, y: BF16 [T, H] with row strides ldx, ldy; y may be x itself (same
+ * pointer and stride).  gamma, beta: FP32 [H], contiguous (the guide's
+ * "gemma" is gamma).  mean, rstd: FP32 [T] or NULL (FP32 statistics, the
+ * mean summed and the deviations squared in FP32 with compensated sums across
+ * threads).  Errors as rmsnorm_fwd; 1 <= H <= CRMSN_MAX_H, H even.
+ */
+crmsn_status layernorm(void *y, int64_t ldy, const void *x, int64_t ldx,
+                       const float *gamma, const float *beta, float eps,
+                       int64_t T, int64_t H, float *mean, float *rstd,
+                       cudaStream_t stream);
+
+/*
+ * layernorm_quant -- [API] layernorm_quant; [GUIDE] 4.
+ *
+ *   out[t,j] = fp8(((x - mean) * rstd * gamma + beta) / scale)
+ *
+ * as layernorm, with the value divided by the device FP32 scale [1] before
+ * the cast to E4M3FN or E5M2 (fp8_kind), saturating.  out: [T, H] bytes with
+ * row stride ldo.  Errors: CRMSN_ERR_DTYPE for another fp8_kind,
+ * CRMSN_ERR_NULL for a NULL scale; the rest as layernorm.
+ */
+crmsn_status layernorm_quant(void *out, int64_t ldo, int fp8_kind,
+                             const void *x, int64_t ldx,
+                             const float *gamma, const float *beta,
+                             const float *scale, float eps,
+                             int64_t T, int64_t H, float *mean, float *rstd,
+                             cudaStream_t stream);
 
 /*
  * rmsnorm_supports -- [API] supports_* helpers; [GUIDE] 6.1

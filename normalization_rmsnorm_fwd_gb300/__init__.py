@@ -11,7 +11,10 @@ from .binding import (  # noqa: F401
     as_rows,
     fused_add_rmsnorm_fp8_block_quant,
     fused_add_rmsnorm_quant,
+    fused_rmsnorm_silu,
     gate_residual_ada_norm_fp8,
+    layernorm,
+    layernorm_quant,
     rmsnorm_bwd,
     rmsnorm_bwd_noalloc,
     rmsnorm_bwd_workspace,

@@ -31,6 +31,9 @@ SIGNATURES = {
     "gate_residual_ada_norm_fp8": (_ST, [_P, _P, _P, _P, _P, _I, _P, _F, _I, _I, _P, _P, _P]),
     "rmsnorm_supports": (_ST, [_I, _INT, _INT]),
     "crmsn_status_str": (ctypes.c_char_p, [_ST]),
+    "fused_rmsnorm_silu": (_ST, [_P, _I, _INT, _P, _I, _P, _INT, _F, _P, _F, _I, _I, _P, _P]),
+    "layernorm": (_ST, [_P, _I, _P, _I, _P, _P, _F, _I, _I, _P, _P, _P]),
+    "layernorm_quant": (_ST, [_P, _I, _INT, _P, _I, _P, _P, _P, _F, _I, _I, _P, _P, _P]),
 }
 
 STATUS = {
@@ -42,7 +45,8 @@ STATUS = {
 OK = 0
 BF16, F32 = 0, 1
 E4M3, E5M2 = 0, 1
-OP_FWD, OP_BWD, OP_QUANT, OP_BLOCK_QUANT, OP_ADA_STYLE, OP_GATED_ADA_FP8 = range(6)
+OP_FWD, OP_BWD, OP_QUANT, OP_BLOCK_QUANT, OP_ADA_STYLE, OP_GATED_ADA_FP8, OP_SILU, OP_LAYERNORM = range(8)
+OUT_BF16, OUT_E4M3 = 0, 1
 MAX_H = 16384
 
 _lock = threading.Lock()

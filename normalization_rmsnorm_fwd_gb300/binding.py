@@ -225,6 +225,74 @@ def gate_residual_ada_norm_fp8(residual, x, gate, w, style, scale, eps: float = 
     return residual, out, gate_out
 
 
+
+def fused_rmsnorm_silu(x, w, eps: float = 1e-6, weight_bias: float = 0.0, out=None,
+                       scale=None, rstd=None):
+    """SiLU(RMSNorm(x) * w_eff): out is BF16 (default, allocated when None) or
+    a float8_e4m3fn tensor, which receives e4m3(silu / scale) (scale None:
+    no scale).  Returns out."""
+    _bf16(x, "x")
+    kind = _weight(w)
+    T, H, ldx = as_rows(x, "x")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+    _need_cuda(out, "out")
+    if out.dtype == torch.bfloat16:
+        fmt = _abi.OUT_BF16
+    elif out.dtype == torch.float8_e4m3fn:
+        fmt = _abi.OUT_E4M3
+    else:
+        raise TypeError("out must be bfloat16 or float8_e4m3fn")
+    _, _, ldo = as_rows(out, "out")
+    s = _scale_tensor(scale, x.device) if (scale is not None and fmt == _abi.OUT_E4M3) else None
+    with torch.cuda.device(x.device):
+        st = _lib().fused_rmsnorm_silu(_ptr(out), ldo, fmt, _ptr(x), ldx, _ptr(w), kind,
+                                       float(weight_bias), _ptr(s), float(eps), T, H,
+                                       _ptr(rstd), _stream(x))
+    check("fused_rmsnorm_silu", st)
+    return out
+
+
+def _ln_params(x, gamma, beta):
+    _bf16(x, "x")
+    for t, name in ((gamma, "gamma"), (beta, "beta")):
+        _need_cuda(t, name)
+        if t.dtype != torch.float32 or t.dim() != 1 or (t.numel() > 1 and t.stride(0) != 1):
+            raise TypeError(f"{name} must be a contiguous 1-D float32 tensor")
+    return as_rows(x, "x")
+
+
+def layernorm(x, gamma, beta, eps: float = 1e-5, out=None, mean=None, rstd=None):
+    """bf16((x - E[x]) / sqrt(Var[x] + eps) * gamma + beta) with the
+    population variance; gamma and beta FP32.  Returns out."""
+    T, H, ldx = _ln_params(x, gamma, beta)
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
+    _bf16(out, "out")
+    _, _, ldo = as_rows(out, "out")
+    with torch.cuda.device(x.device):
+        st = _lib().layernorm(_ptr(out), ldo, _ptr(x), ldx, _ptr(gamma), _ptr(beta), float(eps),
+                              T, H, _ptr(mean), _ptr(rstd), _stream(x))
+    check("layernorm", st)
+    return out
+
+
+def layernorm_quant(out, x, gamma, beta, scale, eps: float = 1e-5, mean=None, rstd=None):
+    """out = fp8(layernorm(x) / scale) with out float8_e4m3fn or
+    float8_e5m2.  Returns out."""
+    T, H, ldx = _ln_params(x, gamma, beta)
+    _need_cuda(out, "out")
+    if out.dtype not in _FP8:
+        raise TypeError("out must be float8_e4m3fn or float8_e5m2")
+    _, _, ldo = as_rows(out, "out")
+    s = _scale_tensor(scale, x.device)
+    with torch.cuda.device(x.device):
+        st = _lib().layernorm_quant(_ptr(out), ldo, _FP8[out.dtype], _ptr(x), ldx, _ptr(gamma),
+                                    _ptr(beta), _ptr(s), float(eps), T, H, _ptr(mean), _ptr(rstd),
+                                    _stream(x))
+    check("layernorm_quant", st)
+    return out
+
 # --------------------------------------------------------------- backward --
 
 def rmsnorm_bwd_workspace_bytes(rows: int, hidden: int, device=None, residual: bool = False) -> int:

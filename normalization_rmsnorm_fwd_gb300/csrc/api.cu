@@ -263,6 +263,11 @@ crmsn_status rmsnorm_supports(int64_t H, int w_dtype, int op)
             if (w_dtype != CRMSN_BF16) return CRMSN_ERR_DTYPE;
             if (H < 1) return CRMSN_ERR_SHAPE;
             return (H % 128 || H > CRMSN_MAX_H) ? CRMSN_ERR_UNSUPPORTED_H : CRMSN_OK;
+        case CRMSN_OP_SILU:
+            return check_h(H);
+        case CRMSN_OP_LAYERNORM:
+            if (w_dtype != CRMSN_F32) return CRMSN_ERR_DTYPE;
+            return check_h(H);
         case CRMSN_OP_ADA_STYLE:
         case CRMSN_OP_GATED_ADA_FP8:
             if (w_dtype != CRMSN_BF16) return CRMSN_ERR_DTYPE;
@@ -527,6 +532,122 @@ crmsn_status gate_residual_ada_norm_fp8(void *residual, const void *x, const voi
 {
     return ada_common(residual, x, gate, w, style, style_rows, scale, eps, T, D, out, gate_out,
                       true, stream);
+}
+
+crmsn_status fused_rmsnorm_silu(void *out, int64_t ldo, int out_format, const void *x,
+                                int64_t ldx, const void *w, int w_dtype, float weight_bias,
+                                const float *scale, float eps, int64_t T, int64_t H,
+                                float *rstd, cudaStream_t stream)
+{
+    if (T < 0) return CRMSN_ERR_SHAPE;
+    if (crmsn_status s = check_h(H)) return s;
+    if (w_dtype != CRMSN_BF16 && w_dtype != CRMSN_F32) return CRMSN_ERR_DTYPE;
+    if (out_format != CRMSN_OUT_BF16 && out_format != CRMSN_OUT_E4M3) return CRMSN_ERR_DTYPE;
+    if (bad_float(eps) || eps < 0.f || bad_float(weight_bias)) return CRMSN_ERR_ARG;
+    if (T == 0) return CRMSN_OK;
+    if (!out || !x || !w) return CRMSN_ERR_NULL;
+    if (T > 1 && (ldo < H || ldx < H)) return CRMSN_ERR_SHAPE;
+    const bool fp8 = out_format == CRMSN_OUT_E4M3;
+    const int wes = w_dtype == CRMSN_F32 ? 4 : 2;
+    const Tensor ts[] = {
+        {{x, T, ldx, H, 2}, false, -1},
+        {{w, 1, H, H, wes}, false, -1},
+        {{fp8 ? scale : nullptr, 1, 1, 1, 4}, false, -1},
+        {{out, T, ldo, H, fp8 ? 1 : 2}, true, fp8 ? -1 : 0},   // BF16 out may replace x
+        {{rstd, 1, T, T, 4}, true, -1},
+    };
+    if (crmsn_status s = check_alias(ts, 5)) return s;
+    const Access acc[] = {{x, ldx, 0}, {out, ldo, fp8 ? 1 : 0},
+                          {w, 0, w_dtype == CRMSN_F32 ? 3 : 2}};
+    const int vec = pick_vec(acc, 3, H, T);
+    if (!vec || (fp8 && scale && !al(scale, 4)) || (rstd && !al(rstd, 4))) return CRMSN_ERR_ALIGNMENT;
+    const Layout L = choose_fwd((int)H, vec, false, false);
+    if ((T + L.rpc - 1) / L.rpc > kMaxBlocks) return CRMSN_ERR_SHAPE;
+
+    FwdParams p{};
+    p.x = static_cast<const uint16_t *>(x); p.ldx = ldx;
+    p.w = w; p.bias = weight_bias; p.eps = eps;
+    p.T = T; p.H = (int)H;
+    p.rstd = rstd;
+    if (fp8) {
+        p.q = static_cast<uint8_t *>(out); p.ldq = ldo;
+        p.scale = scale;
+    } else {
+        p.y = static_cast<uint16_t *>(out); p.ldy = ldo;
+    }
+    p.tpr = L.tpr; p.rpc = L.rpc;
+    return launched(launch_fwd_silu(p, w_dtype == CRMSN_F32, fp8, L, stream));
+}
+
+}  // extern "C"
+
+namespace {
+
+// layernorm (fp8k < 0, BF16 out) and layernorm_quant (fp8k = FP8 kind).
+crmsn_status layernorm_common(void *out, int64_t ldo, int fp8k, const void *x, int64_t ldx,
+                              const float *gamma, const float *beta, const float *scale,
+                              float eps, int64_t T, int64_t H, float *mean, float *rstd,
+                              cudaStream_t stream)
+{
+    if (T < 0) return CRMSN_ERR_SHAPE;
+    if (crmsn_status s = check_h(H)) return s;
+    if (bad_float(eps) || eps < 0.f) return CRMSN_ERR_ARG;
+    if (T == 0) return CRMSN_OK;
+    const bool fp8 = fp8k >= 0;
+    if (!out || !x || !gamma || !beta || (fp8 && !scale)) return CRMSN_ERR_NULL;
+    if (T > 1 && (ldo < H || ldx < H)) return CRMSN_ERR_SHAPE;
+    const Tensor ts[] = {
+        {{x, T, ldx, H, 2}, false, -1},
+        {{gamma, 1, H, H, 4}, false, -1},
+        {{beta, 1, H, H, 4}, false, -1},
+        {{fp8 ? scale : nullptr, 1, 1, 1, 4}, false, -1},
+        {{out, T, ldo, H, fp8 ? 1 : 2}, true, fp8 ? -1 : 0},   // BF16 out may replace x
+        {{mean, 1, T, T, 4}, true, -1},
+        {{rstd, 1, T, T, 4}, true, -1},
+    };
+    if (crmsn_status s = check_alias(ts, 7)) return s;
+    const Access acc[] = {{x, ldx, 0}, {out, ldo, fp8 ? 1 : 0}, {gamma, 0, 3}, {beta, 0, 3}};
+    const int vec = pick_vec(acc, 4, H, T);
+    if (!vec || (fp8 && !al(scale, 4)) || (mean && !al(mean, 4)) || (rstd && !al(rstd, 4)))
+        return CRMSN_ERR_ALIGNMENT;
+    const Layout L = choose_fwd((int)H, vec, false, false);
+    if ((T + L.rpc - 1) / L.rpc > kMaxBlocks) return CRMSN_ERR_SHAPE;
+
+    FwdParams p{};
+    p.x = static_cast<const uint16_t *>(x); p.ldx = ldx;
+    p.w = gamma; p.beta = beta; p.eps = eps;
+    p.T = T; p.H = (int)H;
+    p.rstd = rstd; p.mean = mean;
+    if (fp8) {
+        p.q = static_cast<uint8_t *>(out); p.ldq = ldo;
+        p.scale = scale;
+    } else {
+        p.y = static_cast<uint16_t *>(out); p.ldy = ldo;
+    }
+    p.tpr = L.tpr; p.rpc = L.rpc;
+    return launched(launch_fwd_layernorm(p, fp8k, L, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+crmsn_status layernorm(void *y, int64_t ldy, const void *x, int64_t ldx, const float *gamma,
+                       const float *beta, float eps, int64_t T, int64_t H, float *mean,
+                       float *rstd, cudaStream_t stream)
+{
+    return layernorm_common(y, ldy, -1, x, ldx, gamma, beta, nullptr, eps, T, H, mean, rstd,
+                            stream);
+}
+
+crmsn_status layernorm_quant(void *out, int64_t ldo, int fp8_kind, const void *x, int64_t ldx,
+                             const float *gamma, const float *beta, const float *scale,
+                             float eps, int64_t T, int64_t H, float *mean, float *rstd,
+                             cudaStream_t stream)
+{
+    if (fp8_kind != CRMSN_E4M3 && fp8_kind != CRMSN_E5M2) return CRMSN_ERR_DTYPE;
+    return layernorm_common(out, ldo, fp8_kind, x, ldx, gamma, beta, scale, eps, T, H, mean,
+                            rstd, stream);
 }
 
 }  // extern "C"

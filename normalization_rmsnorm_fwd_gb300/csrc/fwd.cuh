@@ -18,11 +18,26 @@
 //   rstd   = 1 / sqrt(ss / H + eps)        (IEEE sqrt and division)
 //   o      = (h * rstd) * f32(w + bias)
 //   then one of the epilogues below.
+// LayerNorm rows ("FlashInfer normalization operator guide" 4) take the mean
+// first and then the sum of squared deviations (both compensated across
+// threads): rstd = 1 / sqrt(ss_dev / H + eps), o = (h - mean)*rstd*gamma + beta.
 #pragma once
 
 #include "launch.h"
 
 namespace crmsn {
+
+// SiLU(v) = v / (1 + exp(-v)) as v * sigmoid(v) with e = exp(-|v|) in (0, 1]
+// (no overflow for any finite v): sigmoid = 1 / (1 + e) for v >= 0 and
+// e / (1 + e) otherwise.  __expf and the approximate reciprocal of 1 + e (in
+// [1, 2]) keep the relative error near 2^-20 for |v| < 10 and far below a
+// BF16 half-ulp everywhere.
+__device__ __forceinline__ float silu_f32(float v)
+{
+    const float e = __expf(-fabsf(v));
+    const float r = __fdividef(1.0f, 1.0f + e);
+    return v * (v >= 0.f ? r : e * r);
+}
 
 template <int IN, bool W32, int OUT, int FP8K, int VEC, int VPT, bool SUB>
 __global__ void __launch_bounds__(kFwdMaxThreads)
@@ -30,7 +45,9 @@ k_rmsnorm_fwd(const FwdParams p)
 {
     constexpr int NW = VEC / 2;
     constexpr bool ADA = (OUT == OUT_ADA || OUT == OUT_ADA_Q);
+    constexpr bool LN = (IN == IN_LAYERNORM);
     __shared__ float red_h[32], red_l[32];
+    __shared__ float red2_h[LN ? 32 : 1], red2_l[LN ? 32 : 1];
 
     const int tpr = p.tpr;
     const int grp = threadIdx.x / tpr;
@@ -43,14 +60,14 @@ k_rmsnorm_fwd(const FwdParams p)
     BVec<VEC> xa[VPT], ra[VPT], ga[VPT];
     BVec<VEC> sc[VPT], sh[VPT], gt[VPT];
     BVec<VEC> wb[VPT];
-    float wf[VPT][VEC];
+    float wf[VPT][VEC], bt[VPT][VEC];
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = k * tpr + lane;
         if (live && v < nvec) {
             const int64_t c = (int64_t)v * VEC;
             xa[k] = ld_stream<VEC>(p.x + t * p.ldx + c);
-            if constexpr (IN != IN_PLAIN)
+            if constexpr (IN == IN_RESIDUAL || IN == IN_GATED)
                 ra[k] = ld_stream<VEC>(p.r + t * p.ldr + c);
             if constexpr (IN == IN_GATED)
                 ga[k] = ld_stream<VEC>(p.gate + t * p.ldgate + c);
@@ -70,6 +87,7 @@ k_rmsnorm_fwd(const FwdParams p)
                 ld_f32_keep<VEC>(static_cast<const float *>(p.w) + c, wf[k]);
             else
                 wb[k] = ld_keep<VEC>(static_cast<const uint16_t *>(p.w) + c);
+            if constexpr (LN) ld_f32_keep<VEC>(p.beta + c, bt[k]);
         } else {
 #pragma unroll
             for (int i = 0; i < NW; ++i) {
@@ -77,7 +95,7 @@ k_rmsnorm_fwd(const FwdParams p)
                 sc[k].w[i] = 0u; sh[k].w[i] = 0u; gt[k].w[i] = 0u; wb[k].w[i] = 0u;
             }
 #pragma unroll
-            for (int i = 0; i < VEC; ++i) wf[k][i] = 0.f;
+            for (int i = 0; i < VEC; ++i) { wf[k][i] = 0.f; bt[k][i] = 0.f; }
         }
     }
 
@@ -90,7 +108,7 @@ k_rmsnorm_fwd(const FwdParams p)
         for (int i = 0; i < NW; ++i) {
             const uint32_t xw = xa[k].w[i];
             uint32_t hw;
-            if constexpr (IN == IN_PLAIN) {
+            if constexpr (IN == IN_PLAIN || LN) {
                 hw = xw;
             } else if constexpr (IN == IN_RESIDUAL) {
                 // The FP32 sum of two BF16 values rounded once to BF16 is the
@@ -103,11 +121,13 @@ k_rmsnorm_fwd(const FwdParams p)
                 hw = bf16_f2(f2_add(f2_bf16(ra[k].w[i]), f2_bf16(pw)));
             }
             h[k].w[i] = hw;
-            // h^2 is exact in FP32, so the fma rounds only the accumulation.
             const F2 h2 = f2_bf16(hw);
-            ss2 = f2_fma(h2, h2, ss2);
+            if constexpr (LN)
+                ss2 = f2_add(h2, ss2);          // sum of h (the mean comes first)
+            else
+                ss2 = f2_fma(h2, h2, ss2);      // h^2 is exact in FP32: one rounding
         }
-        if constexpr (IN != IN_PLAIN) {
+        if constexpr (IN != IN_PLAIN && !LN) {
             const int v = k * tpr + lane;
             if (live && v < nvec)
                 st_stream<VEC>(p.hn + t * p.ldh + (int64_t)v * VEC, h[k]);
@@ -115,24 +135,46 @@ k_rmsnorm_fwd(const FwdParams p)
     }
 
     // ---------------- phase 3: row reduction -> rstd ----------------------
-    float sh_, sl_;
-    two_sum(f2_lo(ss2), f2_hi(ss2), sh_, sl_);
-    if constexpr (SUB) {
-        pair_reduce_lanes(sh_, sl_, tpr);
-    } else {
-        // Butterfly within each warp, then across the group's warps: short
-        // latency for these short-lived CTAs.
-        pair_reduce_lanes(sh_, sl_, 32);
-        const int nwarp = tpr >> 5;
-        const int warp = threadIdx.x >> 5;
-        if ((threadIdx.x & 31) == 0) {
-            red_h[warp] = sh_;
-            red_l[warp] = sl_;
+    // Compensated sum over the row group of a per-thread FP32 pair: shuffles
+    // within a group of <= 32 threads; otherwise a butterfly within each warp,
+    // then across the group's warps (short latency for these short-lived CTAs).
+    auto row_sum = [&](F2 part, float *rh, float *rl) -> float {
+        float sh_, sl_;
+        two_sum(f2_lo(part), f2_hi(part), sh_, sl_);
+        if constexpr (SUB) {
+            pair_reduce_lanes(sh_, sl_, tpr);
+        } else {
+            pair_reduce_lanes(sh_, sl_, 32);
+            const int nwarp = tpr >> 5;
+            const int warp = threadIdx.x >> 5;
+            if ((threadIdx.x & 31) == 0) {
+                rh[warp] = sh_;
+                rl[warp] = sl_;
+            }
+            __syncthreads();
+            pair_reduce_warps(sh_, sl_, rh, rl, grp * nwarp, nwarp);
         }
-        __syncthreads();
-        pair_reduce_warps(sh_, sl_, red_h, red_l, grp * nwarp, nwarp);
+        return __fadd_rn(sh_, sl_);
+    };
+    float mean = 0.f;
+    if constexpr (LN) {
+        mean = __fdiv_rn(row_sum(ss2, red2_h, red2_l), (float)p.H);
+        // Squared deviations of this thread's elements (none past the row).
+        const F2 nm2 = f2(-mean);
+        ss2 = f2(0.f);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const bool ok = live && k * tpr + lane < nvec;
+#pragma unroll
+            for (int i = 0; i < NW; ++i) {
+                const F2 d = f2_add(f2_bf16(h[k].w[i]), nm2);
+                if (ok) ss2 = f2_fma(d, d, ss2);
+            }
+        }
+        if (p.mean != nullptr && live && lane == 0)
+            p.mean[t] = mean;
     }
-    const float ssum = __fadd_rn(sh_, sl_);
+    const float ssum = row_sum(ss2, red_h, red_l);
     const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ssum, (float)p.H), p.eps)));
     if (p.rstd != nullptr && live && lane == 0)
         p.rstd[t] = rstd;
@@ -141,6 +183,9 @@ k_rmsnorm_fwd(const FwdParams p)
     float scale_v = 1.f;
     if constexpr (OUT == OUT_Q || OUT == OUT_ADA_Q)
         scale_v = __ldg(p.scale);
+    if constexpr (OUT == OUT_SILU_Q)
+        scale_v = p.scale != nullptr ? __ldg(p.scale) : 1.f;
+    const F2 nmean2 = f2(-mean);
     const F2 rstd2 = f2(rstd);
     const F2 bias2 = f2(p.bias);
 
@@ -153,7 +198,11 @@ k_rmsnorm_fwd(const FwdParams p)
 #pragma unroll
         for (int i = 0; i < NW; ++i) {
             const F2 w2 = W32 ? f2(wf[k][2 * i], wf[k][2 * i + 1]) : f2_bf16(wb[k].w[i]);
-            o[i] = f2_mul(f2_mul(f2_bf16(h[k].w[i]), rstd2), f2_add(w2, bias2));
+            if constexpr (LN)
+                o[i] = f2_fma(f2_mul(f2_add(f2_bf16(h[k].w[i]), nmean2), rstd2), w2,
+                              f2(bt[k][2 * i], bt[k][2 * i + 1]));
+            else
+                o[i] = f2_mul(f2_mul(f2_bf16(h[k].w[i]), rstd2), f2_add(w2, bias2));
         }
 
         if constexpr (OUT == OUT_Y) {
@@ -195,6 +244,18 @@ k_rmsnorm_fwd(const FwdParams p)
                 if ((v & 15) == 0)
                     p.bscale[(int64_t)(v >> 4) * p.ldT + t] = s;
             }
+        } else if constexpr (OUT == OUT_SILU) {
+            BVec<VEC> yv;
+#pragma unroll
+            for (int i = 0; i < NW; ++i) yv.w[i] = pack_bf16(silu_f32(f2_lo(o[i])), silu_f32(f2_hi(o[i])));
+            if (ok) st_stream<VEC>(p.y + t * p.ldy + c, yv);
+        } else if constexpr (OUT == OUT_SILU_Q) {
+            uint32_t cq[NW];
+#pragma unroll
+            for (int i = 0; i < NW; ++i)
+                cq[i] = pack_fp8<0>(__fdiv_rn(silu_f32(f2_lo(o[i])), scale_v),
+                                    __fdiv_rn(silu_f32(f2_hi(o[i])), scale_v));
+            if (ok) st_fp8<VEC>(p.q + t * p.ldq + c, cq);
         } else {  // ADA: o * (1 + scale) + shift, one FP32 rounding (fma)
             const F2 one2 = f2(1.f);
             F2 ov[NW];

@@ -21,13 +21,15 @@ constexpr int kBwdMaxCtasPerSm = 2;
 constexpr int kBwdMaxGroups = 4;
 constexpr int kBwdMaxGroupWarps = kBwdMaxThreads / 32;
 
-enum InKind { IN_PLAIN = 0, IN_RESIDUAL = 1, IN_GATED = 2 };
+enum InKind { IN_PLAIN = 0, IN_RESIDUAL = 1, IN_GATED = 2, IN_LAYERNORM = 3 };
 enum OutKind {
     OUT_Y = 0,         // y = bf16(o)
     OUT_Q = 1,         // q = fp8(o / scale)
     OUT_BLOCK = 2,     // normed = bf16(o); 1x128 block FP8 + block scales
     OUT_ADA = 3,       // out = bf16(o * (1 + sc) + sh); gate_out copy
-    OUT_ADA_Q = 4      // out = e4m3((o * (1 + sc) + sh) / scale); gate_out copy
+    OUT_ADA_Q = 4,     // out = e4m3((o * (1 + sc) + sh) / scale); gate_out copy
+    OUT_SILU = 5,      // y = bf16(silu(o))
+    OUT_SILU_Q = 6     // q = e4m3(silu(o) / scale), scale 1 when p.scale is NULL
 };
 
 struct FwdParams {
@@ -44,6 +46,8 @@ struct FwdParams {
     float *bscale;       int64_t ldT;     // block scales [H/128][ldT]
     const uint16_t *style; int64_t lds;   // style row stride (0: broadcast)
     uint16_t *gate_out;  int64_t ldgo;
+    const float *beta;                    // LayerNorm shift [H] (w is gamma)
+    float *mean;                          // LayerNorm row means (nullable)
     int tpr;             int rpc;
 };
 
@@ -71,6 +75,10 @@ cudaError_t launch_fwd_y(const FwdParams &p, int in, bool w32, const Layout &L, 
 cudaError_t launch_fwd_q(const FwdParams &p, int in, bool w32, int fp8k, const Layout &L, cudaStream_t s);
 cudaError_t launch_fwd_block(const FwdParams &p, const Layout &L, cudaStream_t s);
 cudaError_t launch_fwd_ada(const FwdParams &p, bool gated_fp8, const Layout &L, cudaStream_t s);
+// RMSNorm + SiLU (BF16, or E4M3 when fp8) and LayerNorm (BF16 when
+// fp8k < 0, else FP8 of that kind), fwd_silu_ln.cu.
+cudaError_t launch_fwd_silu(const FwdParams &p, bool w32, bool fp8, const Layout &L, cudaStream_t s);
+cudaError_t launch_fwd_layernorm(const FwdParams &p, int fp8k, const Layout &L, cudaStream_t s);
 
 // Backward (bwd.cu).
 // Picks the chunk count (resident CTAs per SM x sms, at most

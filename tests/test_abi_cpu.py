@@ -150,3 +150,36 @@ def test_supports(L):
     assert L.rmsnorm_supports(3072, 0, 5) == OK
     assert L.rmsnorm_supports(3071, 0, 4) == SHAPE
     assert L.rmsnorm_supports(3072, 0, 9) == ARG
+
+
+def test_silu_and_layernorm_validation(L):
+    silu = lambda **kw: L.fused_rmsnorm_silu(
+        kw.get("out", A), 256, kw.get("fmt", 0), kw.get("x", A + 64 * MB), 256, A + 128 * MB,
+        kw.get("wd", 0), 0.0, kw.get("scale", None), 1e-6, 4, kw.get("H", 256), None, None)
+    assert silu(fmt=2) == DTYPE
+    assert silu(wd=3) == DTYPE
+    assert silu(H=255) == UNSUP
+    assert silu(out=A + 64 * MB + 2) == ALIAS        # partial overlap with x
+    assert silu(out=A + 64 * MB) == CUDA             # in place over x is allowed
+    assert silu(fmt=1, out=A + 64 * MB) == ALIAS     # an FP8 out cannot replace x
+    assert silu(fmt=1) == CUDA                       # no scale: the plain cast
+    assert silu(x=None) == NULL
+    ln = lambda **kw: L.layernorm(
+        kw.get("y", A), 256, kw.get("x", A + 64 * MB), 256, kw.get("g", A + 128 * MB),
+        kw.get("b", A + 129 * MB), kw.get("eps", 1e-5), 4, kw.get("H", 256), None, None, None)
+    assert ln(b=None) == NULL
+    assert ln(eps=-1.0) == ARG
+    assert ln(H=0) == SHAPE
+    assert ln(g=A + 128 * MB + 4) == ALIGN           # 4-byte aligned: the 8-element path
+    assert ln(g=A + 128 * MB + 2) == ALIGN
+    assert ln(y=A + 64 * MB) == CUDA
+    assert ln() == CUDA
+    lq = lambda **kw: L.layernorm_quant(
+        A, 256, kw.get("kind", 0), A + 64 * MB, 256, A + 128 * MB, A + 129 * MB,
+        kw.get("scale", A + 130 * MB), 1e-5, 4, 256, None, None, None)
+    assert lq(kind=2) == DTYPE
+    assert lq(scale=None) == NULL
+    assert lq(kind=1) == CUDA
+    assert L.rmsnorm_supports(1024, 0, 6) == OK
+    assert L.rmsnorm_supports(1024, 1, 7) == OK
+    assert L.rmsnorm_supports(1024, 0, 7) == DTYPE

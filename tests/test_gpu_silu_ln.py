@@ -1,0 +1,197 @@
+"""RMSNorm + SiLU and LayerNorm on the GPU against the oracle, element by
+element: BF16 outputs within one BF16 ulp of the exact value (plus a
+cancellation allowance for LayerNorm's + beta), FP8 codes equal except one
+code next to a rounding midpoint, FP32 statistics within a few FP32 ulps."""
+import numpy as np
+import pytest
+import torch
+
+import gpu_util as gu
+import oracle
+from normalization_rmsnorm_fwd_gb300 import synth
+import normalization_rmsnorm_fwd_gb300 as crm
+
+pytestmark = pytest.mark.gpu
+
+SILU_H = [2, 64, 128, 160, 256, 320, 512, 640, 1024, 2048, 4096, 8192, 16384]
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.Oracle()
+
+
+def _silu_gpu(x, w, bias=0.0, fp8=False, scale=None, out=None):
+    xd = gu.dev_bf16(x)
+    wd = gu.dev_f32(w) if w.dtype == np.float32 else gu.dev_bf16(w)
+    if out is None and fp8:
+        out = torch.empty(xd.shape, dtype=torch.float8_e4m3fn, device="cuda")
+    rstd = torch.empty(x.shape[0], dtype=torch.float32, device="cuda")
+    y = crm.fused_rmsnorm_silu(xd, wd, 1e-6, weight_bias=bias, out=out, scale=scale, rstd=rstd)
+    torch.cuda.synchronize()
+    return y, rstd
+
+
+def _check_silu(orc, x, w, bias=0.0, rows=None):
+    y, rstd = _silu_gpu(x, w, bias)
+    xs = x if rows is None else x[rows]
+    ref = orc.fused_rmsnorm_silu(xs, w, 1e-6, weight_bias=bias)
+    got = gu.host_bits(y)
+    got = got if rows is None else got[rows]
+    gu.check_bf16(got, ref["v_exact"], what="silu bf16")
+    r = rstd.cpu().numpy()
+    gu.check_rstd(r if rows is None else r[rows], ref["rstd"].astype(np.float64))
+    for scale in (None, 0.04):
+        q, _ = _silu_gpu(x, w, bias, fp8=True, scale=scale)
+        refq = orc.fused_rmsnorm_silu(xs, w, 1e-6, weight_bias=bias, fp8=True,
+                                      scale=1.0 if scale is None else scale)
+        gq = gu.host_u8(q)
+        gu.check_fp8(gq if rows is None else gq[rows], refq["q"], refq["v_exact"], 0,
+                     what=f"silu e4m3 scale={scale}")
+
+
+@pytest.mark.parametrize("H", SILU_H)
+def test_silu_widths(orc, H):
+    x = synth.random_rows(H + 1, 67, H)[0]
+    _check_silu(orc, x, synth.random_weight(H + 1, H))
+
+
+@pytest.mark.parametrize("route", ["gemma", "f32"])
+def test_silu_weight_routes(orc, route):
+    H = 640
+    x = synth.random_rows(7, 300, H)[0]
+    w = synth.random_weight(7, H, f32=route == "f32")
+    _check_silu(orc, x, w, bias=1.0)
+
+
+@pytest.mark.parametrize("T", [1, 2, 7, 63, 257, 1560])
+def test_silu_row_counts(orc, T):
+    x = synth.random_rows(T, T, 160)[0]
+    _check_silu(orc, x, synth.random_weight(T, 160))
+
+
+def test_silu_large_sampled(orc):
+    # The largest point of the B200 sweep grid, T = 399360, H = 1024, checked
+    # on sampled rows (the op is row-independent).
+    T, H = 399360, 1024
+    gen = torch.Generator().manual_seed(3)
+    x = synth.bf16_bits(torch.randn(T, H, generator=gen))
+    _check_silu(orc, x, synth.random_weight(3, H), rows=gu.sample_rows(T))
+
+
+def test_silu_in_place_and_strided(orc):
+    H = 256
+    buf = synth.random_rows(9, 40, 2 * H)[0]
+    x = buf[:, :H]                        # row stride 2H
+    w = synth.random_weight(9, H)
+    xd = gu.dev_bf16(buf)[:, :H]
+    crm.fused_rmsnorm_silu(xd, gu.dev_bf16(w), 1e-6, out=xd)
+    torch.cuda.synchronize()
+    ref = orc.fused_rmsnorm_silu(np.ascontiguousarray(x), w, 1e-6)
+    gu.check_bf16(gu.host_bits(xd), ref["v_exact"], what="silu in place, strided")
+
+
+def test_silu_extreme_values(orc):
+    # Rows whose normalised values reach +-60 (a few large entries): SiLU of
+    # large negative values underflows towards -0, of large positive ones is v.
+    H = 128
+    gen = torch.Generator().manual_seed(11)
+    v = torch.randn(16, H, generator=gen) * 0.01
+    v[:, 0] = 60.0
+    v[:, 1] = -60.0
+    v[:8, 2] = -3.0
+    x = synth.bf16_bits(v)
+    w = synth.bf16_bits(torch.full((H,), 8.0))
+    _check_silu(orc, x, w)
+
+
+# ---------------------------------------------------------------- LayerNorm --
+
+def _gamma_beta(seed, H):
+    gen = torch.Generator().manual_seed(seed)
+    gamma = (1 + 0.1 * torch.randn(H, generator=gen)).numpy().astype(np.float32)
+    beta = (0.1 * torch.randn(H, generator=gen)).numpy().astype(np.float32)
+    return gamma, beta
+
+
+def _ln_allowance(x, ref, gamma, beta):
+    h = x.astype(np.float64)
+    d = np.abs(h - ref["mean"][:, None]) + np.abs(ref["mean"][:, None])
+    return 2.0 ** -20 * (d * ref["rstd"][:, None] * np.abs(gamma) + np.abs(beta))
+
+
+def _check_ln(orc, x, gamma, beta, eps=1e-5, rows=None, kinds=(0, 1)):
+    xd = gu.dev_bf16(x)
+    gd, bd = gu.dev_f32(gamma), gu.dev_f32(beta)
+    T = x.shape[0]
+    mean = torch.empty(T, dtype=torch.float32, device="cuda")
+    rstd = torch.empty(T, dtype=torch.float32, device="cuda")
+    y = crm.layernorm(xd, gd, bd, eps, mean=mean, rstd=rstd)
+    torch.cuda.synchronize()
+    sel = slice(None) if rows is None else rows
+    xs = x[sel]
+    ref = orc.layernorm(xs, gamma, beta, eps)
+    xdec = orc.bf16_to_f64(xs)
+    allow = _ln_allowance(xdec, ref, gamma, beta)
+    gu.check_bf16(gu.host_bits(y)[sel], ref["v_exact"], allowance=allow, what="layernorm")
+    gu.check_rstd(rstd.cpu().numpy()[sel], ref["rstd"])
+    m = mean.cpu().numpy()[sel].astype(np.float64)
+    scale_m = np.abs(xdec).mean(axis=1)
+    assert np.all(np.abs(m - ref["mean"]) <= 2.0 ** -22 * scale_m + 1e-30), "mean"
+    for kind in kinds:
+        dt = torch.float8_e4m3fn if kind == 0 else torch.float8_e5m2
+        q = torch.empty(xd.shape, dtype=dt, device="cuda")
+        crm.layernorm_quant(q, xd, gd, bd, 0.04, eps)
+        torch.cuda.synchronize()
+        rq = orc.layernorm(xs, gamma, beta, eps, fp8_kind=kind, scale=0.04)
+        gu.check_fp8(gu.host_u8(q)[sel], rq["q"], rq["v_exact"], kind,
+                     what=f"layernorm_quant kind={kind}",
+                     allowance=allow / float(np.float32(0.04)))
+
+
+@pytest.mark.parametrize("H", [2, 64, 160, 256, 1000, 2048, 3072, 4096, 5120, 8192, 16384])
+def test_layernorm_widths(orc, H):
+    x = synth.random_rows(H + 2, 45, H)[0]
+    g, b = _gamma_beta(H, H)
+    _check_ln(orc, x, g, b)
+
+
+@pytest.mark.parametrize("T", [1, 3, 64, 129, 4097])
+def test_layernorm_row_counts(orc, T):
+    x = synth.random_rows(T + 5, T, 768)[0]
+    g, b = _gamma_beta(T, 768)
+    _check_ln(orc, x, g, b, rows=None if T < 1000 else gu.sample_rows(T))
+
+
+def test_layernorm_offset_rows(orc):
+    # A large common offset: the mean dominates and the deviations are small
+    # (the case a one-pass sum of squares gets wrong).
+    H = 1024
+    gen = torch.Generator().manual_seed(5)
+    v = 300.0 + torch.randn(32, H, generator=gen)
+    x = synth.bf16_bits(v)
+    g, b = _gamma_beta(5, H)
+    _check_ln(orc, x, g, b, eps=1e-6)
+
+
+def test_layernorm_constant_row(orc):
+    # A constant row has zero variance: the output is beta exactly.
+    H = 512
+    x = synth.bf16_bits(torch.full((4, H), 3.25))
+    g, b = _gamma_beta(6, H)
+    y = crm.layernorm(gu.dev_bf16(x), gu.dev_f32(g), gu.dev_f32(b), 1e-5)
+    torch.cuda.synchronize()
+    assert np.array_equal(gu.host_bits(y), orc.bf16_from_f64(b.astype(np.float64)[None, :].repeat(4, 0)))
+
+
+def test_layernorm_strided_in_place(orc):
+    H = 128
+    buf = synth.random_rows(12, 64, 3 * H)[0]
+    g, b = _gamma_beta(12, H)
+    xd = gu.dev_bf16(buf)[:, H:2 * H]
+    crm.layernorm(xd, gu.dev_f32(g), gu.dev_f32(b), 1e-5, out=xd)
+    torch.cuda.synchronize()
+    xs = np.ascontiguousarray(buf[:, H:2 * H])
+    ref = orc.layernorm(xs, g, b, 1e-5)
+    allow = _ln_allowance(orc.bf16_to_f64(xs), ref, g, b)
+    gu.check_bf16(gu.host_bits(xd), ref["v_exact"], allowance=allow, what="layernorm in place")
