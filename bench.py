@@ -269,6 +269,34 @@ def other_kernels(dev, peak):
     add("ada_rms_norm_style broadcast style T=2520 D=3072", ada(1), 46_473_216)
     add("gate_residual_ada_norm_fp8 per-row style T=2520 D=3072", gated(T), 131_610_628)
     add("gate_residual_ada_norm_fp8 broadcast style T=2520 D=3072", gated(1), 85_180_420)
+
+    # RMSNorm + SiLU at the largest and a small-H point of the B200 sweep grid
+    # (H in 64..1024, T in 1560..399360): read x, write y (BF16) or q (E4M3).
+    def silu(Ts, H, fp8):
+        def make():
+            x, w = randn(Ts, H), randn(H, scale=0.1, shift=1.0)
+            o = torch.empty((Ts, H), dtype=torch.float8_e4m3fn if fp8 else torch.bfloat16,
+                            device=dev)
+            return lambda: crm.fused_rmsnorm_silu(x, w, out=o)
+        return make
+    for Ts, H in ((399360, 1024), (399360, 128)):
+        add(f"fused_rmsnorm_silu bf16 T={Ts} H={H}", silu(Ts, H, False), Ts * H * 4 + H * 2)
+    add("fused_rmsnorm_silu e4m3 T=399360 H=1024", silu(399360, 1024, True),
+        399360 * 1024 * 3 + 1024 * 2)
+
+    # LayerNorm at the headline shape: read x, write y (BF16) or q (E4M3).
+    def ln(fp8):
+        def make():
+            x = randn(16384, 4096)
+            g, b = 1 + 0.1 * torch.randn(4096, device=dev), 0.1 * torch.randn(4096, device=dev)
+            if fp8:
+                q = torch.empty((16384, 4096), dtype=torch.float8_e4m3fn, device=dev)
+                return lambda: crm.layernorm_quant(q, x, g, b, sc)
+            y = torch.empty_like(x)
+            return lambda: crm.layernorm(x, g, b, out=y)
+        return make
+    add("layernorm bf16 T=16384 H=4096", ln(False), 16384 * 4096 * 4 + 4096 * 8)
+    add("layernorm_quant e4m3 T=16384 H=4096", ln(True), 16384 * 4096 * 3 + 4096 * 8 + 4)
     return out
 
 

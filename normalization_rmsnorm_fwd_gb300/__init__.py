@@ -23,3 +23,4 @@ from .binding import (  # noqa: F401
     rmsnorm_quant,
     rmsnorm_supports,
 )
+from .autograd import RMSNormFunction, rmsnorm  # noqa: F401,E402
