@@ -46,10 +46,10 @@ int next_pow2(int v)
 // at most); wider rows use a group of whole warps, at most 16, holding 2 or 4
 // 16-byte vectors (2..16 4-byte vectors) per thread, choosing the fewest idle
 // lanes (ties: the first preference).  The Ada epilogues stream three more
-// tensors per element and prefer fewer vectors per thread.  Narrow groups
-// share a CTA so that CTAs have about 256 threads.  need16: the 1x128 block
-// epilogue needs 16-lane aligned groups.
-Layout choose_fwd(int H, int vec, bool need16, bool ada)
+// tensors per element and prefer fewer vectors per thread (narrow).  Narrow
+// groups share a CTA so that CTAs have about 256 threads.  need16: the 1x128 block epilogue needs
+// 16-lane aligned groups.
+Layout choose_fwd(int H, int vec, bool need16, bool narrow)
 {
     const int nvec = H / vec;
     Layout L{};
@@ -64,9 +64,10 @@ Layout choose_fwd(int H, int vec, bool need16, bool ada)
         L.rpc = 256 / tpr;
         return L;
     }
-    static const int prefs8[] = {4, 2}, prefs8_ada[] = {2, 4};
-    static const int prefs2[] = {16, 8, 4, 2}, prefs2_ada[] = {8, 4, 16, 2};
-    const int *prefs = vec == 8 ? (ada ? prefs8_ada : prefs8) : (ada ? prefs2_ada : prefs2);
+    static const int prefs8[] = {4, 2}, prefs8_narrow[] = {2, 4};
+    static const int prefs2[] = {16, 8, 4, 2}, prefs2_narrow[] = {8, 4, 16, 2};
+    const int *prefs = vec == 8 ? (narrow ? prefs8_narrow : prefs8)
+                                : (narrow ? prefs2_narrow : prefs2);
     const int np = vec == 8 ? 2 : 4;
     int best = -1;
     long best_waste = 0;

@@ -21,7 +21,16 @@
 // LayerNorm rows ("FlashInfer normalization operator guide" 4) take the mean
 // first and then the sum of squared deviations (both compensated across
 // threads): rstd = 1 / sqrt(ss_dev / H + eps), o = (h - mean)*rstd*gamma + beta.
+//
+// Two launch forms.  One row per group per CTA (LOOP = false): a grid of
+// ceil(T / rpc) CTAs.  Persistent (LOOP = true, the plain row with the y or
+// static FP8 epilogue, which streams a single input): a grid of resident CTAs
+// whose groups walk the rows with a stride of the whole grid; the weights are
+// loaded once per CTA and the next row's x is loaded before the current row
+// is reduced and written, so its loads are in flight during that work.
 #pragma once
+
+#include <atomic>
 
 #include "launch.h"
 
@@ -39,7 +48,7 @@ __device__ __forceinline__ float silu_f32(float v)
     return v * (v >= 0.f ? r : e * r);
 }
 
-template <int IN, bool W32, int OUT, int FP8K, int VEC, int VPT, bool SUB>
+template <int IN, bool W32, int OUT, int FP8K, int VEC, int VPT, bool SUB, bool LOOP>
 __global__ void __launch_bounds__(kFwdMaxThreads)
 k_rmsnorm_fwd(const FwdParams p)
 {
@@ -52,37 +61,16 @@ k_rmsnorm_fwd(const FwdParams p)
     const int tpr = p.tpr;
     const int grp = threadIdx.x / tpr;
     const int lane = threadIdx.x - grp * tpr;
-    const int64_t t = (int64_t)blockIdx.x * p.rpc + grp;
-    const bool live = t < p.T;
     const int nvec = p.H / VEC;
 
-    // ---------------- phase 1: issue every load of the row ----------------
-    BVec<VEC> xa[VPT], ra[VPT], ga[VPT];
-    BVec<VEC> sc[VPT], sh[VPT], gt[VPT];
+    // ---------------- phase 1: loads ---------------------------------------
+    // Weights (and LayerNorm's beta): row-independent.
     BVec<VEC> wb[VPT];
     float wf[VPT][VEC], bt[VPT][VEC];
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
+    auto load_weight_vec = [&](int k) {
         const int v = k * tpr + lane;
-        if (live && v < nvec) {
+        if (v < nvec) {
             const int64_t c = (int64_t)v * VEC;
-            xa[k] = ld_stream<VEC>(p.x + t * p.ldx + c);
-            if constexpr (IN == IN_RESIDUAL || IN == IN_GATED)
-                ra[k] = ld_stream<VEC>(p.r + t * p.ldr + c);
-            if constexpr (IN == IN_GATED)
-                ga[k] = ld_stream<VEC>(p.gate + t * p.ldgate + c);
-            if constexpr (ADA) {
-                const uint16_t *srow = p.style + t * p.lds;
-                if (p.lds == 0) {
-                    sc[k] = ld_keep<VEC>(srow + c);
-                    sh[k] = ld_keep<VEC>(srow + p.H + c);
-                    gt[k] = ld_keep<VEC>(srow + 2 * p.H + c);
-                } else {
-                    sc[k] = ld_stream<VEC>(srow + c);
-                    sh[k] = ld_stream<VEC>(srow + p.H + c);
-                    gt[k] = ld_stream<VEC>(srow + 2 * p.H + c);
-                }
-            }
             if constexpr (W32)
                 ld_f32_keep<VEC>(static_cast<const float *>(p.w) + c, wf[k]);
             else
@@ -90,202 +78,294 @@ k_rmsnorm_fwd(const FwdParams p)
             if constexpr (LN) ld_f32_keep<VEC>(p.beta + c, bt[k]);
         } else {
 #pragma unroll
-            for (int i = 0; i < NW; ++i) {
-                xa[k].w[i] = 0u; ra[k].w[i] = 0u; ga[k].w[i] = 0u;
-                sc[k].w[i] = 0u; sh[k].w[i] = 0u; gt[k].w[i] = 0u; wb[k].w[i] = 0u;
-            }
+            for (int i = 0; i < NW; ++i) wb[k].w[i] = 0u;
 #pragma unroll
             for (int i = 0; i < VEC; ++i) { wf[k][i] = 0.f; bt[k][i] = 0.f; }
         }
-    }
-
-    // ---------------- phase 2: normalised input h, sum of squares ---------
-    BVec<VEC> h[VPT];
-    F2 ss2 = f2(0.f);
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-#pragma unroll
-        for (int i = 0; i < NW; ++i) {
-            const uint32_t xw = xa[k].w[i];
-            uint32_t hw;
-            if constexpr (IN == IN_PLAIN || LN) {
-                hw = xw;
-            } else if constexpr (IN == IN_RESIDUAL) {
-                // The FP32 sum of two BF16 values rounded once to BF16 is the
-                // correctly rounded BF16 sum (double rounding is innocuous).
-                hw = bf16_f2(f2_add(f2_bf16(xw), f2_bf16(ra[k].w[i])));
-            } else {
-                // bf16(x * gate) first (the FP32 product of two BF16 values is
-                // exact), then the BF16 residual add.
-                const uint32_t pw = bf16_f2(f2_mul(f2_bf16(xw), f2_bf16(ga[k].w[i])));
-                hw = bf16_f2(f2_add(f2_bf16(ra[k].w[i]), f2_bf16(pw)));
-            }
-            h[k].w[i] = hw;
-            const F2 h2 = f2_bf16(hw);
-            if constexpr (LN)
-                ss2 = f2_add(h2, ss2);          // sum of h (the mean comes first)
-            else
-                ss2 = f2_fma(h2, h2, ss2);      // h^2 is exact in FP32: one rounding
-        }
-        if constexpr (IN != IN_PLAIN && !LN) {
-            const int v = k * tpr + lane;
-            if (live && v < nvec)
-                st_stream<VEC>(p.hn + t * p.ldh + (int64_t)v * VEC, h[k]);
-        }
-    }
-
-    // ---------------- phase 3: row reduction -> rstd ----------------------
-    // Compensated sum over the row group of a per-thread FP32 pair: shuffles
-    // within a group of <= 32 threads; otherwise a butterfly within each warp,
-    // then across the group's warps (short latency for these short-lived CTAs).
-    auto row_sum = [&](F2 part, float *rh, float *rl) -> float {
-        float sh_, sl_;
-        two_sum(f2_lo(part), f2_hi(part), sh_, sl_);
-        if constexpr (SUB) {
-            pair_reduce_lanes(sh_, sl_, tpr);
-        } else {
-            pair_reduce_lanes(sh_, sl_, 32);
-            const int nwarp = tpr >> 5;
-            const int warp = threadIdx.x >> 5;
-            if ((threadIdx.x & 31) == 0) {
-                rh[warp] = sh_;
-                rl[warp] = sl_;
-            }
-            __syncthreads();
-            pair_reduce_warps(sh_, sl_, rh, rl, grp * nwarp, nwarp);
-        }
-        return __fadd_rn(sh_, sl_);
     };
-    float mean = 0.f;
-    if constexpr (LN) {
-        mean = __fdiv_rn(row_sum(ss2, red2_h, red2_l), (float)p.H);
-        // Squared deviations of this thread's elements (none past the row).
-        const F2 nm2 = f2(-mean);
-        ss2 = f2(0.f);
+    auto load_weights = [&]() {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) load_weight_vec(k);
+    };
+    // The row's streamed inputs: x (into xs), residual, gate, style, and with
+    // `weights` the weight vectors too (interleaved per vector: fewer live
+    // registers than all of one tensor first).
+    BVec<VEC> xa[VPT], ra[VPT], ga[VPT];
+    BVec<VEC> sc[VPT], sh[VPT], gt[VPT];
+    auto load_row = [&](int64_t t, BVec<VEC> (&xs)[VPT], bool weights) {
+        const bool live = t < p.T;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
-            const bool ok = live && k * tpr + lane < nvec;
-#pragma unroll
-            for (int i = 0; i < NW; ++i) {
-                const F2 d = f2_add(f2_bf16(h[k].w[i]), nm2);
-                if (ok) ss2 = f2_fma(d, d, ss2);
-            }
-        }
-        if (p.mean != nullptr && live && lane == 0)
-            p.mean[t] = mean;
-    }
-    const float ssum = row_sum(ss2, red_h, red_l);
-    const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ssum, (float)p.H), p.eps)));
-    if (p.rstd != nullptr && live && lane == 0)
-        p.rstd[t] = rstd;
-
-    // ---------------- phase 4: epilogue -----------------------------------
-    float scale_v = 1.f;
-    if constexpr (OUT == OUT_Q || OUT == OUT_ADA_Q)
-        scale_v = __ldg(p.scale);
-    if constexpr (OUT == OUT_SILU_Q)
-        scale_v = p.scale != nullptr ? __ldg(p.scale) : 1.f;
-    const F2 nmean2 = f2(-mean);
-    const F2 rstd2 = f2(rstd);
-    const F2 bias2 = f2(p.bias);
-
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-        const int v = k * tpr + lane;
-        const bool ok = live && v < nvec;
-        const int64_t c = (int64_t)v * VEC;
-        F2 o[NW];
-#pragma unroll
-        for (int i = 0; i < NW; ++i) {
-            const F2 w2 = W32 ? f2(wf[k][2 * i], wf[k][2 * i + 1]) : f2_bf16(wb[k].w[i]);
-            if constexpr (LN)
-                o[i] = f2_fma(f2_mul(f2_add(f2_bf16(h[k].w[i]), nmean2), rstd2), w2,
-                              f2(bt[k][2 * i], bt[k][2 * i + 1]));
-            else
-                o[i] = f2_mul(f2_mul(f2_bf16(h[k].w[i]), rstd2), f2_add(w2, bias2));
-        }
-
-        if constexpr (OUT == OUT_Y) {
-            BVec<VEC> yv;
-#pragma unroll
-            for (int i = 0; i < NW; ++i) yv.w[i] = bf16_f2(o[i]);
-            if (ok) st_stream<VEC>(p.y + t * p.ldy + c, yv);
-        } else if constexpr (OUT == OUT_Q) {
-            uint32_t cq[NW];
-#pragma unroll
-            for (int i = 0; i < NW; ++i)
-                cq[i] = pack_fp8<FP8K>(__fdiv_rn(f2_lo(o[i]), scale_v), __fdiv_rn(f2_hi(o[i]), scale_v));
-            if (ok) st_fp8<VEC>(p.q + t * p.ldq + c, cq);
-        } else if constexpr (OUT == OUT_BLOCK) {
-            // normed = bf16(o); amax over the 128-column block held by 16
-            // consecutive lanes (VEC == 8, tpr a multiple of 16).
-            BVec<VEC> nv;
-            float amax = 0.f;
-#pragma unroll
-            for (int i = 0; i < NW; ++i) {
-                nv.w[i] = bf16_f2(o[i]);
-                amax = fmaxf(amax, fmaxf(fabsf(bf_lo(nv.w[i])), fabsf(bf_hi(nv.w[i]))));
-            }
-            if (ok) st_stream<VEC>(p.y + t * p.ldy + c, nv);
-#pragma unroll
-            for (int off = 8; off > 0; off >>= 1)
-                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-            const float s = __fdiv_rn(amax, 448.0f);
-            uint32_t cq[NW];
-#pragma unroll
-            for (int i = 0; i < NW; ++i) {
-                if (s > 0.f)
-                    cq[i] = pack_fp8<0>(__fdiv_rn(bf_lo(nv.w[i]), s), __fdiv_rn(bf_hi(nv.w[i]), s));
-                else
-                    cq[i] = 0u;
-            }
-            if (ok) {
-                st_fp8<VEC>(p.q + t * p.ldq + c, cq);
-                if ((v & 15) == 0)
-                    p.bscale[(int64_t)(v >> 4) * p.ldT + t] = s;
-            }
-        } else if constexpr (OUT == OUT_SILU) {
-            BVec<VEC> yv;
-#pragma unroll
-            for (int i = 0; i < NW; ++i) yv.w[i] = pack_bf16(silu_f32(f2_lo(o[i])), silu_f32(f2_hi(o[i])));
-            if (ok) st_stream<VEC>(p.y + t * p.ldy + c, yv);
-        } else if constexpr (OUT == OUT_SILU_Q) {
-            uint32_t cq[NW];
-#pragma unroll
-            for (int i = 0; i < NW; ++i)
-                cq[i] = pack_fp8<0>(__fdiv_rn(silu_f32(f2_lo(o[i])), scale_v),
-                                    __fdiv_rn(silu_f32(f2_hi(o[i])), scale_v));
-            if (ok) st_fp8<VEC>(p.q + t * p.ldq + c, cq);
-        } else {  // ADA: o * (1 + scale) + shift, one FP32 rounding (fma)
-            const F2 one2 = f2(1.f);
-            F2 ov[NW];
-#pragma unroll
-            for (int i = 0; i < NW; ++i)
-                ov[i] = f2_fma(o[i], f2_add(one2, f2_bf16(sc[k].w[i])), f2_bf16(sh[k].w[i]));
-            if constexpr (OUT == OUT_ADA) {
-                BVec<VEC> out;
-#pragma unroll
-                for (int i = 0; i < NW; ++i) out.w[i] = bf16_f2(ov[i]);
-                if (ok) st_stream<VEC>(p.y + t * p.ldy + c, out);
+            if (weights) load_weight_vec(k);
+            const int v = k * tpr + lane;
+            if (live && v < nvec) {
+                const int64_t c = (int64_t)v * VEC;
+                xs[k] = ld_stream<VEC>(p.x + t * p.ldx + c);
+                if constexpr (IN == IN_RESIDUAL || IN == IN_GATED)
+                    ra[k] = ld_stream<VEC>(p.r + t * p.ldr + c);
+                if constexpr (IN == IN_GATED)
+                    ga[k] = ld_stream<VEC>(p.gate + t * p.ldgate + c);
+                if constexpr (ADA) {
+                    const uint16_t *srow = p.style + t * p.lds;
+                    if (p.lds == 0) {
+                        sc[k] = ld_keep<VEC>(srow + c);
+                        sh[k] = ld_keep<VEC>(srow + p.H + c);
+                        gt[k] = ld_keep<VEC>(srow + 2 * p.H + c);
+                    } else {
+                        sc[k] = ld_stream<VEC>(srow + c);
+                        sh[k] = ld_stream<VEC>(srow + p.H + c);
+                        gt[k] = ld_stream<VEC>(srow + 2 * p.H + c);
+                    }
+                }
             } else {
-                uint32_t cq[NW];
 #pragma unroll
-                for (int i = 0; i < NW; ++i)
-                    cq[i] = pack_fp8<0>(__fdiv_rn(f2_lo(ov[i]), scale_v), __fdiv_rn(f2_hi(ov[i]), scale_v));
-                if (ok) st_fp8<VEC>(p.q + t * p.ldq + c, cq);
+                for (int i = 0; i < NW; ++i) {
+                    xs[k].w[i] = 0u; ra[k].w[i] = 0u; ga[k].w[i] = 0u;
+                    sc[k].w[i] = 0u; sh[k].w[i] = 0u; gt[k].w[i] = 0u;
+                }
             }
-            if (ok) st_stream<VEC>(p.gate_out + t * p.ldgo + c, gt[k]);
+        }
+    };
+
+    // Phases 2-4 of row t, whose inputs are in xa (and ra, ga, sc, sh, gt).
+    // Every thread of the CTA calls it the same number of times (it may
+    // contain CTA barriers).
+    auto process = [&](int64_t t) {
+        const bool live = t < p.T;
+        // ---------------- phase 2: normalised input h, sum of squares ---------
+        BVec<VEC> h[VPT];
+        F2 ss2 = f2(0.f);
+    #pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+    #pragma unroll
+            for (int i = 0; i < NW; ++i) {
+                const uint32_t xw = xa[k].w[i];
+                uint32_t hw;
+                if constexpr (IN == IN_PLAIN || LN) {
+                    hw = xw;
+                } else if constexpr (IN == IN_RESIDUAL) {
+                    // The FP32 sum of two BF16 values rounded once to BF16 is the
+                    // correctly rounded BF16 sum (double rounding is innocuous).
+                    hw = bf16_f2(f2_add(f2_bf16(xw), f2_bf16(ra[k].w[i])));
+                } else {
+                    // bf16(x * gate) first (the FP32 product of two BF16 values is
+                    // exact), then the BF16 residual add.
+                    const uint32_t pw = bf16_f2(f2_mul(f2_bf16(xw), f2_bf16(ga[k].w[i])));
+                    hw = bf16_f2(f2_add(f2_bf16(ra[k].w[i]), f2_bf16(pw)));
+                }
+                h[k].w[i] = hw;
+                const F2 h2 = f2_bf16(hw);
+                if constexpr (LN)
+                    ss2 = f2_add(h2, ss2);          // sum of h (the mean comes first)
+                else
+                    ss2 = f2_fma(h2, h2, ss2);      // h^2 is exact in FP32: one rounding
+            }
+            if constexpr (IN != IN_PLAIN && !LN) {
+                const int v = k * tpr + lane;
+                if (live && v < nvec)
+                    st_stream<VEC>(p.hn + t * p.ldh + (int64_t)v * VEC, h[k]);
+            }
+        }
+
+        // ---------------- phase 3: row reduction -> rstd ----------------------
+        // Compensated sum over the row group of a per-thread FP32 pair: shuffles
+        // within a group of <= 32 threads; otherwise a butterfly within each warp,
+        // then across the group's warps (short latency for these short-lived CTAs).
+        auto row_sum = [&](F2 part, float *rh, float *rl) -> float {
+            float sh_, sl_;
+            two_sum(f2_lo(part), f2_hi(part), sh_, sl_);
+            if constexpr (SUB) {
+                pair_reduce_lanes(sh_, sl_, tpr);
+            } else {
+                pair_reduce_lanes(sh_, sl_, 32);
+                const int nwarp = tpr >> 5;
+                const int warp = threadIdx.x >> 5;
+                if ((threadIdx.x & 31) == 0) {
+                    rh[warp] = sh_;
+                    rl[warp] = sl_;
+                }
+                __syncthreads();
+                pair_reduce_warps(sh_, sl_, rh, rl, grp * nwarp, nwarp);
+            }
+            return __fadd_rn(sh_, sl_);
+        };
+        float mean = 0.f;
+        if constexpr (LN) {
+            mean = __fdiv_rn(row_sum(ss2, red2_h, red2_l), (float)p.H);
+            // Squared deviations of this thread's elements (none past the row).
+            const F2 nm2 = f2(-mean);
+            ss2 = f2(0.f);
+    #pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const bool ok = live && k * tpr + lane < nvec;
+    #pragma unroll
+                for (int i = 0; i < NW; ++i) {
+                    const F2 d = f2_add(f2_bf16(h[k].w[i]), nm2);
+                    if (ok) ss2 = f2_fma(d, d, ss2);
+                }
+            }
+            if (p.mean != nullptr && live && lane == 0)
+                p.mean[t] = mean;
+        }
+        const float ssum = row_sum(ss2, red_h, red_l);
+        const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ssum, (float)p.H), p.eps)));
+        if (p.rstd != nullptr && live && lane == 0)
+            p.rstd[t] = rstd;
+
+        // ---------------- phase 4: epilogue -----------------------------------
+        float scale_v = 1.f;
+        if constexpr (OUT == OUT_Q || OUT == OUT_ADA_Q)
+            scale_v = __ldg(p.scale);
+        if constexpr (OUT == OUT_SILU_Q)
+            scale_v = p.scale != nullptr ? __ldg(p.scale) : 1.f;
+        const F2 nmean2 = f2(-mean);
+        const F2 rstd2 = f2(rstd);
+        const F2 bias2 = f2(p.bias);
+
+    #pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = k * tpr + lane;
+            const bool ok = live && v < nvec;
+            const int64_t c = (int64_t)v * VEC;
+            F2 o[NW];
+    #pragma unroll
+            for (int i = 0; i < NW; ++i) {
+                const F2 w2 = W32 ? f2(wf[k][2 * i], wf[k][2 * i + 1]) : f2_bf16(wb[k].w[i]);
+                if constexpr (LN)
+                    o[i] = f2_fma(f2_mul(f2_add(f2_bf16(h[k].w[i]), nmean2), rstd2), w2,
+                                  f2(bt[k][2 * i], bt[k][2 * i + 1]));
+                else
+                    o[i] = f2_mul(f2_mul(f2_bf16(h[k].w[i]), rstd2), f2_add(w2, bias2));
+            }
+
+            if constexpr (OUT == OUT_Y) {
+                BVec<VEC> yv;
+    #pragma unroll
+                for (int i = 0; i < NW; ++i) yv.w[i] = bf16_f2(o[i]);
+                if (ok) st_stream<VEC>(p.y + t * p.ldy + c, yv);
+            } else if constexpr (OUT == OUT_Q) {
+                uint32_t cq[NW];
+    #pragma unroll
+                for (int i = 0; i < NW; ++i)
+                    cq[i] = pack_fp8<FP8K>(__fdiv_rn(f2_lo(o[i]), scale_v), __fdiv_rn(f2_hi(o[i]), scale_v));
+                if (ok) st_fp8<VEC>(p.q + t * p.ldq + c, cq);
+            } else if constexpr (OUT == OUT_BLOCK) {
+                // normed = bf16(o); amax over the 128-column block held by 16
+                // consecutive lanes (VEC == 8, tpr a multiple of 16).
+                BVec<VEC> nv;
+                float amax = 0.f;
+    #pragma unroll
+                for (int i = 0; i < NW; ++i) {
+                    nv.w[i] = bf16_f2(o[i]);
+                    amax = fmaxf(amax, fmaxf(fabsf(bf_lo(nv.w[i])), fabsf(bf_hi(nv.w[i]))));
+                }
+                if (ok) st_stream<VEC>(p.y + t * p.ldy + c, nv);
+    #pragma unroll
+                for (int off = 8; off > 0; off >>= 1)
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+                const float s = __fdiv_rn(amax, 448.0f);
+                uint32_t cq[NW];
+    #pragma unroll
+                for (int i = 0; i < NW; ++i) {
+                    if (s > 0.f)
+                        cq[i] = pack_fp8<0>(__fdiv_rn(bf_lo(nv.w[i]), s), __fdiv_rn(bf_hi(nv.w[i]), s));
+                    else
+                        cq[i] = 0u;
+                }
+                if (ok) {
+                    st_fp8<VEC>(p.q + t * p.ldq + c, cq);
+                    if ((v & 15) == 0)
+                        p.bscale[(int64_t)(v >> 4) * p.ldT + t] = s;
+                }
+            } else if constexpr (OUT == OUT_SILU) {
+                BVec<VEC> yv;
+    #pragma unroll
+                for (int i = 0; i < NW; ++i) yv.w[i] = pack_bf16(silu_f32(f2_lo(o[i])), silu_f32(f2_hi(o[i])));
+                if (ok) st_stream<VEC>(p.y + t * p.ldy + c, yv);
+            } else if constexpr (OUT == OUT_SILU_Q) {
+                uint32_t cq[NW];
+    #pragma unroll
+                for (int i = 0; i < NW; ++i)
+                    cq[i] = pack_fp8<0>(__fdiv_rn(silu_f32(f2_lo(o[i])), scale_v),
+                                        __fdiv_rn(silu_f32(f2_hi(o[i])), scale_v));
+                if (ok) st_fp8<VEC>(p.q + t * p.ldq + c, cq);
+            } else {  // ADA: o * (1 + scale) + shift, one FP32 rounding (fma)
+                const F2 one2 = f2(1.f);
+                F2 ov[NW];
+    #pragma unroll
+                for (int i = 0; i < NW; ++i)
+                    ov[i] = f2_fma(o[i], f2_add(one2, f2_bf16(sc[k].w[i])), f2_bf16(sh[k].w[i]));
+                if constexpr (OUT == OUT_ADA) {
+                    BVec<VEC> out;
+    #pragma unroll
+                    for (int i = 0; i < NW; ++i) out.w[i] = bf16_f2(ov[i]);
+                    if (ok) st_stream<VEC>(p.y + t * p.ldy + c, out);
+                } else {
+                    uint32_t cq[NW];
+    #pragma unroll
+                    for (int i = 0; i < NW; ++i)
+                        cq[i] = pack_fp8<0>(__fdiv_rn(f2_lo(ov[i]), scale_v), __fdiv_rn(f2_hi(ov[i]), scale_v));
+                    if (ok) st_fp8<VEC>(p.q + t * p.ldq + c, cq);
+                }
+                if (ok) st_stream<VEC>(p.gate_out + t * p.ldgo + c, gt[k]);
+            }
+        }
+    };
+
+    if constexpr (!LOOP) {
+        const int64_t t = (int64_t)blockIdx.x * p.rpc + grp;
+        load_row(t, xa, true);
+        process(t);
+    } else {
+        static_assert(IN == IN_PLAIN, "the persistent form streams one input");
+        load_weights();
+        const int64_t stride = (int64_t)gridDim.x * p.rpc;
+        const int64_t b0 = (int64_t)blockIdx.x * p.rpc;
+        load_row(b0 + grp, xa, false);
+        for (int64_t base = b0; base < p.T; base += stride) {
+            BVec<VEC> xn[VPT];
+            const bool more = base + stride < p.T;   // the same for the whole CTA
+            if (more) load_row(base + stride + grp, xn, false);
+            process(base + grp);
+            if (more) {
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) xa[k] = xn[k];
+            }
         }
     }
 }
 
-// Host-side launch of one instantiation.
+// Host-side launch of one instantiation.  The single-input variants run the
+// persistent form on at most (resident CTAs per SM) x (SMs) CTAs; the
+// residency of a block size is computed once and remembered.
 template <int IN, bool W32, int OUT, int FP8K, int VEC, int VPT, bool SUB>
 cudaError_t launch_fwd_inst(const FwdParams &p, cudaStream_t s)
 {
+    // Measured: the persistent form pays off for the plain row with the y and
+    // static FP8 epilogues; SiLU (bound by its arithmetic) and LayerNorm
+    // (gamma and beta) run faster in the one-row form.
+    constexpr bool LOOP = IN == IN_PLAIN && (OUT == OUT_Y || OUT == OUT_Q);
+    auto kern = k_rmsnorm_fwd<IN, W32, OUT, FP8K, VEC, VPT, SUB, LOOP>;
     const int threads = p.tpr * p.rpc;
-    const int64_t blocks = (p.T + p.rpc - 1) / p.rpc;
-    k_rmsnorm_fwd<IN, W32, OUT, FP8K, VEC, VPT, SUB><<<(unsigned)blocks, threads, 0, s>>>(p);
+    int64_t blocks = (p.T + p.rpc - 1) / p.rpc;
+    if constexpr (LOOP) {
+        static std::atomic<long long> cached{0};   // threads << 32 | CTAs per SM
+        long long c = cached.load(std::memory_order_relaxed);
+        int per_sm = (int)(c & 0xffffffff);
+        if ((c >> 32) != threads || per_sm <= 0) {
+            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
+            if (e != cudaSuccess) return e;
+            if (per_sm < 1) per_sm = 1;
+            cached.store(((long long)threads << 32) | per_sm, std::memory_order_relaxed);
+        }
+        int dev = 0, sms = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        const int64_t cap = (int64_t)per_sm * sms;
+        if (blocks > cap) blocks = cap;
+    }
+    kern<<<(unsigned)blocks, threads, 0, s>>>(p);
     return cudaGetLastError();
 }
 
