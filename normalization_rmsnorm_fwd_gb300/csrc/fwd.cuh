@@ -64,10 +64,14 @@ k_rmsnorm_fwd(const FwdParams p)
     const int nvec = p.H / VEC;
 
     // ---------------- phase 1: loads ---------------------------------------
-    // Weights (and LayerNorm's beta): row-independent.
+    // Weights (and LayerNorm's beta): row-independent.  LayerNorm loads gamma
+    // and beta in its epilogue instead, vector by vector, so that they do not
+    // hold registers through the two reductions.
+    constexpr bool LN_LATE = LN;
     BVec<VEC> wb[VPT];
     float wf[VPT][VEC], bt[VPT][VEC];
     auto load_weight_vec = [&](int k) {
+        if constexpr (LN_LATE) return;
         const int v = k * tpr + lane;
         if (v < nvec) {
             const int64_t c = (int64_t)v * VEC;
@@ -135,9 +139,9 @@ k_rmsnorm_fwd(const FwdParams p)
         // ---------------- phase 2: normalised input h, sum of squares ---------
         BVec<VEC> h[VPT];
         F2 ss2 = f2(0.f);
-    #pragma unroll
+#pragma unroll
         for (int k = 0; k < VPT; ++k) {
-    #pragma unroll
+#pragma unroll
             for (int i = 0; i < NW; ++i) {
                 const uint32_t xw = xa[k].w[i];
                 uint32_t hw;
@@ -195,10 +199,10 @@ k_rmsnorm_fwd(const FwdParams p)
             // Squared deviations of this thread's elements (none past the row).
             const F2 nm2 = f2(-mean);
             ss2 = f2(0.f);
-    #pragma unroll
+#pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const bool ok = live && k * tpr + lane < nvec;
-    #pragma unroll
+#pragma unroll
                 for (int i = 0; i < NW; ++i) {
                     const F2 d = f2_add(f2_bf16(h[k].w[i]), nm2);
                     if (ok) ss2 = f2_fma(d, d, ss2);
@@ -222,13 +226,22 @@ k_rmsnorm_fwd(const FwdParams p)
         const F2 rstd2 = f2(rstd);
         const F2 bias2 = f2(p.bias);
 
-    #pragma unroll
+#pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = k * tpr + lane;
             const bool ok = live && v < nvec;
             const int64_t c = (int64_t)v * VEC;
+            if constexpr (LN_LATE) {
+                if (v < nvec) {
+                    ld_f32_keep<VEC>(static_cast<const float *>(p.w) + c, wf[k]);
+                    ld_f32_keep<VEC>(p.beta + c, bt[k]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) { wf[k][i] = 0.f; bt[k][i] = 0.f; }
+                }
+            }
             F2 o[NW];
-    #pragma unroll
+#pragma unroll
             for (int i = 0; i < NW; ++i) {
                 const F2 w2 = W32 ? f2(wf[k][2 * i], wf[k][2 * i + 1]) : f2_bf16(wb[k].w[i]);
                 if constexpr (LN)
@@ -240,12 +253,12 @@ k_rmsnorm_fwd(const FwdParams p)
 
             if constexpr (OUT == OUT_Y) {
                 BVec<VEC> yv;
-    #pragma unroll
+#pragma unroll
                 for (int i = 0; i < NW; ++i) yv.w[i] = bf16_f2(o[i]);
                 if (ok) st_stream<VEC>(p.y + t * p.ldy + c, yv);
             } else if constexpr (OUT == OUT_Q) {
                 uint32_t cq[NW];
-    #pragma unroll
+#pragma unroll
                 for (int i = 0; i < NW; ++i)
                     cq[i] = pack_fp8<FP8K>(__fdiv_rn(f2_lo(o[i]), scale_v), __fdiv_rn(f2_hi(o[i]), scale_v));
                 if (ok) st_fp8<VEC>(p.q + t * p.ldq + c, cq);
@@ -254,18 +267,18 @@ k_rmsnorm_fwd(const FwdParams p)
                 // consecutive lanes (VEC == 8, tpr a multiple of 16).
                 BVec<VEC> nv;
                 float amax = 0.f;
-    #pragma unroll
+#pragma unroll
                 for (int i = 0; i < NW; ++i) {
                     nv.w[i] = bf16_f2(o[i]);
                     amax = fmaxf(amax, fmaxf(fabsf(bf_lo(nv.w[i])), fabsf(bf_hi(nv.w[i]))));
                 }
                 if (ok) st_stream<VEC>(p.y + t * p.ldy + c, nv);
-    #pragma unroll
+#pragma unroll
                 for (int off = 8; off > 0; off >>= 1)
                     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
                 const float s = __fdiv_rn(amax, 448.0f);
                 uint32_t cq[NW];
-    #pragma unroll
+#pragma unroll
                 for (int i = 0; i < NW; ++i) {
                     if (s > 0.f)
                         cq[i] = pack_fp8<0>(__fdiv_rn(bf_lo(nv.w[i]), s), __fdiv_rn(bf_hi(nv.w[i]), s));
@@ -279,30 +292,36 @@ k_rmsnorm_fwd(const FwdParams p)
                 }
             } else if constexpr (OUT == OUT_SILU) {
                 BVec<VEC> yv;
-    #pragma unroll
+#pragma unroll
                 for (int i = 0; i < NW; ++i) yv.w[i] = pack_bf16(silu_f32(f2_lo(o[i])), silu_f32(f2_hi(o[i])));
                 if (ok) st_stream<VEC>(p.y + t * p.ldy + c, yv);
             } else if constexpr (OUT == OUT_SILU_Q) {
                 uint32_t cq[NW];
-    #pragma unroll
-                for (int i = 0; i < NW; ++i)
-                    cq[i] = pack_fp8<0>(__fdiv_rn(silu_f32(f2_lo(o[i])), scale_v),
-                                        __fdiv_rn(silu_f32(f2_hi(o[i])), scale_v));
+                if (p.scale == nullptr) {      // the plain cast (no division by 1)
+#pragma unroll
+                    for (int i = 0; i < NW; ++i)
+                        cq[i] = pack_fp8<0>(silu_f32(f2_lo(o[i])), silu_f32(f2_hi(o[i])));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < NW; ++i)
+                        cq[i] = pack_fp8<0>(__fdiv_rn(silu_f32(f2_lo(o[i])), scale_v),
+                                            __fdiv_rn(silu_f32(f2_hi(o[i])), scale_v));
+                }
                 if (ok) st_fp8<VEC>(p.q + t * p.ldq + c, cq);
             } else {  // ADA: o * (1 + scale) + shift, one FP32 rounding (fma)
                 const F2 one2 = f2(1.f);
                 F2 ov[NW];
-    #pragma unroll
+#pragma unroll
                 for (int i = 0; i < NW; ++i)
                     ov[i] = f2_fma(o[i], f2_add(one2, f2_bf16(sc[k].w[i])), f2_bf16(sh[k].w[i]));
                 if constexpr (OUT == OUT_ADA) {
                     BVec<VEC> out;
-    #pragma unroll
+#pragma unroll
                     for (int i = 0; i < NW; ++i) out.w[i] = bf16_f2(ov[i]);
                     if (ok) st_stream<VEC>(p.y + t * p.ldy + c, out);
                 } else {
                     uint32_t cq[NW];
-    #pragma unroll
+#pragma unroll
                     for (int i = 0; i < NW; ++i)
                         cq[i] = pack_fp8<0>(__fdiv_rn(f2_lo(ov[i]), scale_v), __fdiv_rn(f2_hi(ov[i]), scale_v));
                     if (ok) st_fp8<VEC>(p.q + t * p.ldq + c, cq);
