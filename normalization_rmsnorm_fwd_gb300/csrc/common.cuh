@@ -87,6 +87,57 @@ __device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c)
 }
 // Packed BF16 pair -> FP32 pair (exact).
 __device__ __forceinline__ F2 f2_bf16(uint32_t w) { return f2(bf_lo(w), bf_hi(w)); }
+
+// ------------------------------------------------------ division by a scale --
+// v / s rounded to nearest (the IEEE quotient) for a pair v and one divisor s
+// whose reciprocal r = RN(1/s) is known, in five packed instructions:
+// q = RN(v*r), then twice q = RN(q + (v - s*q)*r) with the remainder v - s*q
+// formed exactly by a fused multiply-add.  Markstein's theorem (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990): when r is the correctly rounded
+// reciprocal and q is within one ulp of v/s, the remainder is exact and the
+// corrected quotient is correctly rounded; the first correction brings
+// RN(v*r) (within 1.5 ulps) within one ulp.  This needs the quotient and the
+// remainder to be normal FP32 numbers (the packed instructions flush
+// subnormal results).
+__device__ __forceinline__ F2 f2_div_recip(F2 v, float s, float r)
+{
+    const F2 ns = f2(-s), r2 = f2(r);
+    F2 q = f2_mul(v, r2);
+    F2 e = f2_fma(q, ns, v);
+    q = f2_fma(e, r2, q);
+    e = f2_fma(q, ns, v);
+    return f2_fma(e, r2, q);
+}
+
+// Division of FP8 epilogue values by one scale s.  For |s| in [2^-60, 2^60]
+// the quotient is the IEEE quotient v / s whenever |v| >= 2^-96 and the
+// quotient is finite; a smaller dividend has a quotient below 2^-36, which
+// every FP8 format rounds to zero whatever its last bits, and a quotient
+// beyond the FP32 range (a dividend of 2^68 or more: a normalised value of
+// magnitude <= sqrt(H) times a weight of 2^61 or more) comes out as NaN
+// instead of an infinity.  Other scales use the IEEE division itself.
+struct DivScale {
+    float s, r;
+    bool fast;
+    __device__ __forceinline__ explicit DivScale(float s_) : s(s_), r(0.f), fast(false)
+    {
+        const float a = fabsf(s_);
+        fast = a >= 0x1p-60f && a <= 0x1p60f;
+        if (fast) r = __frcp_rn(s_);
+    }
+    __device__ __forceinline__ void div(F2 v, float &lo, float &hi) const
+    {
+        if (fast) {
+            const F2 q = f2_div_recip(v, s, r);
+            lo = f2_lo(q);
+            hi = f2_hi(q);
+        } else {
+            lo = __fdiv_rn(f2_lo(v), s);
+            hi = __fdiv_rn(f2_hi(v), s);
+        }
+    }
+};
 // FP32 pair -> packed BF16 pair, round to nearest even.
 __device__ __forceinline__ uint32_t bf16_f2(F2 a) { return pack_bf16(f2_lo(a), f2_hi(a)); }
 

@@ -222,6 +222,7 @@ k_rmsnorm_fwd(const FwdParams p)
             scale_v = __ldg(p.scale);
         if constexpr (OUT == OUT_SILU_Q)
             scale_v = p.scale != nullptr ? __ldg(p.scale) : 1.f;
+        const DivScale dsc(scale_v);            // IEEE division by the scale
         const F2 nmean2 = f2(-mean);
         const F2 rstd2 = f2(rstd);
         const F2 bias2 = f2(p.bias);
@@ -259,8 +260,11 @@ k_rmsnorm_fwd(const FwdParams p)
             } else if constexpr (OUT == OUT_Q) {
                 uint32_t cq[NW];
 #pragma unroll
-                for (int i = 0; i < NW; ++i)
-                    cq[i] = pack_fp8<FP8K>(__fdiv_rn(f2_lo(o[i]), scale_v), __fdiv_rn(f2_hi(o[i]), scale_v));
+                for (int i = 0; i < NW; ++i) {
+                    float a, b;
+                    dsc.div(o[i], a, b);
+                    cq[i] = pack_fp8<FP8K>(a, b);
+                }
                 if (ok) st_fp8<VEC>(p.q + t * p.ldq + c, cq);
             } else if constexpr (OUT == OUT_BLOCK) {
                 // normed = bf16(o); amax over the 128-column block held by 16
@@ -277,13 +281,17 @@ k_rmsnorm_fwd(const FwdParams p)
                 for (int off = 8; off > 0; off >>= 1)
                     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
                 const float s = __fdiv_rn(amax, 448.0f);
+                const DivScale bdiv(s);
                 uint32_t cq[NW];
 #pragma unroll
                 for (int i = 0; i < NW; ++i) {
-                    if (s > 0.f)
-                        cq[i] = pack_fp8<0>(__fdiv_rn(bf_lo(nv.w[i]), s), __fdiv_rn(bf_hi(nv.w[i]), s));
-                    else
+                    if (s > 0.f) {
+                        float a, b;
+                        bdiv.div(f2_bf16(nv.w[i]), a, b);
+                        cq[i] = pack_fp8<0>(a, b);
+                    } else {
                         cq[i] = 0u;
+                    }
                 }
                 if (ok) {
                     st_fp8<VEC>(p.q + t * p.ldq + c, cq);
@@ -322,8 +330,11 @@ k_rmsnorm_fwd(const FwdParams p)
                 } else {
                     uint32_t cq[NW];
 #pragma unroll
-                    for (int i = 0; i < NW; ++i)
-                        cq[i] = pack_fp8<0>(__fdiv_rn(f2_lo(ov[i]), scale_v), __fdiv_rn(f2_hi(ov[i]), scale_v));
+                    for (int i = 0; i < NW; ++i) {
+                        float a, b;
+                        dsc.div(ov[i], a, b);
+                        cq[i] = pack_fp8<0>(a, b);
+                    }
                     if (ok) st_fp8<VEC>(p.q + t * p.ldq + c, cq);
                 }
                 if (ok) st_stream<VEC>(p.gate_out + t * p.ldgo + c, gt[k]);
