@@ -135,8 +135,12 @@ k_rmsnorm_bwd(const BwdParams p)
     float *comb = wsm + VPT * tpr * VEC;
     const int wplane = VPT * tpr * 4;
 
+    // This thread's slot of vector k of a tensor in a stage; the per-thread
+    // base and the strides are computed once.
+    unsigned char *const my_slot = ring + (size_t)threadIdx.x * VB;
+    const int kstride = nthr * VB;
     auto slot = [&](int stage, int tensor, int k) -> unsigned char * {
-        return ring + (size_t)stage * stage_bytes + ((size_t)(tensor * VPT + k) * nthr + threadIdx.x) * VB;
+        return my_slot + (size_t)stage * stage_bytes + (tensor * VPT + k) * kstride;
     };
     auto w_at = [&](int v, int i) -> float * {
         if constexpr (VEC == 8) return wsm + (i < 4 ? 0 : wplane) + v * 4 + (i & 3);
@@ -153,34 +157,44 @@ k_rmsnorm_bwd(const BwdParams p)
             we[0] = f2(a.x, a.y);
         }
     };
-    // Issue the copies of iteration `it` (row r0 + grp + it*rpc) into its stage.
-    auto issue = [&](int64_t it) {
-        const int64_t t = r0 + grp + it * rpc;
-        if (t < r1) {
-            const int stage = (int)(it % S);
+    // Copies of the iterations in order: issue_next() issues iteration
+    // `iss` (row r0 + grp + iss*rpc) into stage iss % S and advances; the
+    // source pointers of this thread's first vector move by a row step.
+    int64_t iss = 0, t_iss = r0 + grp;
+    const uint16_t *g_iss = p.g + t_iss * p.ldg + (int64_t)lane * VEC;
+    const uint16_t *x_iss = p.x + t_iss * p.ldx + (int64_t)lane * VEC;
+    const uint16_t *r_iss = GRES ? p.gres + t_iss * p.ldgr + (int64_t)lane * VEC : nullptr;
+    int st_iss = 0;
+    auto issue_next = [&]() {
+        if (t_iss < r1) {
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
-                const int v = k * tpr + lane;
-                if (v < nvec) {
-                    const int64_t c = (int64_t)v * VEC;
+                if (k * tpr + lane < nvec) {
+                    const int c = k * tpr * VEC;
                     if constexpr (VEC == 8) {
-                        cp_async_16(slot(stage, 0, k), p.g + t * p.ldg + c);
-                        cp_async_16(slot(stage, 1, k), p.x + t * p.ldx + c);
-                        if constexpr (GRES) cp_async_16(slot(stage, 2, k), p.gres + t * p.ldgr + c);
+                        cp_async_16(slot(st_iss, 0, k), g_iss + c);
+                        cp_async_16(slot(st_iss, 1, k), x_iss + c);
+                        if constexpr (GRES) cp_async_16(slot(st_iss, 2, k), r_iss + c);
                     } else {
-                        cp_async_4(slot(stage, 0, k), p.g + t * p.ldg + c);
-                        cp_async_4(slot(stage, 1, k), p.x + t * p.ldx + c);
-                        if constexpr (GRES) cp_async_4(slot(stage, 2, k), p.gres + t * p.ldgr + c);
+                        cp_async_4(slot(st_iss, 0, k), g_iss + c);
+                        cp_async_4(slot(st_iss, 1, k), x_iss + c);
+                        if constexpr (GRES) cp_async_4(slot(st_iss, 2, k), r_iss + c);
                     }
                 }
             }
         }
         cp_async_commit();   // one group per iteration, empty or not
+        ++iss;
+        t_iss += rpc;
+        g_iss += (int64_t)rpc * p.ldg;
+        x_iss += (int64_t)rpc * p.ldx;
+        if constexpr (GRES) r_iss += (int64_t)rpc * p.ldgr;
+        st_iss = st_iss + 1 == S ? 0 : st_iss + 1;
     };
 
     // Prologue: the first D rows go in flight while the weight is prepared.
 #pragma unroll
-    for (int i = 0; i < D; ++i) issue(i);
+    for (int i = 0; i < D; ++i) issue_next();
 
     // Effective weight f32(w + bias) of this thread's columns, in shared
     // memory; group 0 writes it, the other groups read it after a barrier.
@@ -298,7 +312,7 @@ k_rmsnorm_bwd(const BwdParams p)
     // Vector k of row t: dx = rstd*(g*w) - x*(rstd^3*m) (+ g_residual), and
     // with with_dw the dw terms g*x*rstd (g*x is exact in FP32) into the block
     // sums.
-    auto dx_vec = [&](bool with_dw, int64_t t, int stage, int k, const F2 (&we)[NW], F2 rs2, F2 nc3) {
+    auto dx_vec = [&](bool with_dw, uint16_t *dxrow, int stage, int k, const F2 (&we)[NW], F2 rs2, F2 nc3) {
         const int v = k * tpr + lane;
         const BVec<VEC> gv = ld_smem_vec<VEC>(slot(stage, 0, k));
         const BVec<VEC> xv = ld_smem_vec<VEC>(slot(stage, 1, k));
@@ -314,11 +328,14 @@ k_rmsnorm_bwd(const BwdParams p)
             o.w[e] = bf16_f2(d2);
             if (with_dw) blk[k][e] = f2_fma(f2_mul(g2, x2), rs2, blk[k][e]);
         }
-        if (v < nvec) st_stream<VEC>(p.dx + t * p.lddx + (int64_t)v * VEC, o);
+        if (v < nvec) st_stream<VEC>(dxrow + k * tpr * VEC, o);
     };
     // rstd*1 and -rstd^3*m for a row with rstd rs and sum of g*w*x `sum`.
+    // m = sum / H as sum * RN(1/H): exact for a power-of-two H, within one
+    // FP32 ulp otherwise (m only scales dx's small second term).
+    const float inv_h = __frcp_rn((float)p.H);
     auto coefs = [&](float rs, float sum, F2 &rs2, F2 &nc3) {
-        const float m = __fdiv_rn(sum, (float)p.H);
+        const float m = __fmul_rn(sum, inv_h);
         rs2 = f2(rs);
         nc3 = f2(-__fmul_rn(__fmul_rn(__fmul_rn(rs, rs), rs), m));
     };
@@ -341,10 +358,25 @@ k_rmsnorm_bwd(const BwdParams p)
             for (int o = 16; o > 0; o >>= 1) sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, o));
             if ((lane & 31) == 0) wsum[((int)(i & 1) * kBwdMaxGroups + grp) * kBwdMaxGroupWarps + wg] = sum;
         };
+        // Sum of the group's warp slots in a fixed pairwise tree over 8 slots
+        // (groups of at most 8 warps) or 16; the unused slots hold zeros.
+        const bool narrow_group = tpr <= 256;
         auto group_total = [&](int64_t i) -> float {
             const float4 *q = reinterpret_cast<const float4 *>(
                 wsum + ((int)(i & 1) * kBwdMaxGroups + grp) * kBwdMaxGroupWarps);
             float v[kBwdMaxGroupWarps];
+            if (narrow_group) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float4 f = q[j];
+                    v[4 * j] = f.x; v[4 * j + 1] = f.y; v[4 * j + 2] = f.z; v[4 * j + 3] = f.w;
+                }
+#pragma unroll
+                for (int w = 1; w < 8; w <<= 1)
+#pragma unroll
+                    for (int j = 0; j + w < 8; j += 2 * w) v[j] = __fadd_rn(v[j], v[j + w]);
+                return v[0];
+            }
 #pragma unroll
             for (int j = 0; j < kBwdMaxGroupWarps / 4; ++j) {
                 const float4 f = q[j];
@@ -375,15 +407,17 @@ k_rmsnorm_bwd(const BwdParams p)
         }
         __syncthreads();
         float tot = group_total(0);
+        int64_t t = r0 + grp;                // row of iteration it
+        uint16_t *dxrow = p.dx + t * p.lddx + (int64_t)lane * VEC;
+        int st = 0;                          // its stage
         for (int64_t it = 0; it < iters; ++it) {
-            issue(it + D);
+            issue_next();                    // iteration it + D
             cp_async_wait<D - 1>();          // this thread's copies of rows it, it+1 landed
             const float rs = rs_of(it, it);
             const F2 rsn2 = f2(rs_of(it + 1, it));
-            const int64_t t = r0 + grp + it * rpc;
             const bool live = t < r1;
             const bool live_n = t + rpc < r1;
-            const int st = (int)(it % S), st_n = (int)((it + 1) % S);
+            const int st_n = st + 1 == S ? 0 : st + 1;
             F2 rs2, nc3;
             coefs(rs, tot, rs2, nc3);
             F2 dot2 = f2(0.f);
@@ -392,22 +426,26 @@ k_rmsnorm_bwd(const BwdParams p)
                 F2 we[NW];
                 ld_w(k, we);
                 if (live_n) dot_dw_vec(st_n, k, we, rsn2, dot2);
-                if (live) dx_vec(false, t, st, k, we, rs2, nc3);
+                if (live) dx_vec(false, dxrow, st, k, we, rs2, nc3);
             }
             publish(it + 1, dot2);
             if ((it + 2) % kDwBlock == 0) fold();
             rs_advance(it);
+            t += rpc;
+            dxrow += (int64_t)rpc * p.lddx;
+            st = st_n;
             __syncthreads();
             tot = group_total(it + 1);
         }
     } else {
+        int64_t t = r0 + grp;                // row of iteration it
+        uint16_t *dxrow = p.dx + t * p.lddx + (int64_t)lane * VEC;
+        int st = 0;                          // its stage
         for (int64_t it = 0; it < iters; ++it) {
-            issue(it + D);                   // keep D rows ahead in flight
+            issue_next();                    // iteration it + D: keep D rows ahead in flight
             cp_async_wait<D>();              // this thread's copies of row `it` landed
             const float rs = rs_of(it, it);
-            const int64_t t = r0 + grp + it * rpc;
             const bool live = t < r1;
-            const int st = (int)(it % S);
             F2 dot2 = f2(0.f);
             if (live) {
 #pragma unroll
@@ -430,11 +468,14 @@ k_rmsnorm_bwd(const BwdParams p)
                 for (int k = 0; k < VPT; ++k) {
                     F2 we[NW];
                     ld_w(k, we);
-                    dx_vec(true, t, st, k, we, rs2, nc3);
+                    dx_vec(true, dxrow, st, k, we, rs2, nc3);
                 }
             }
             if ((it + 1) % kDwBlock == 0) fold();
             rs_advance(it);
+            t += rpc;
+            dxrow += (int64_t)rpc * p.lddx;
+            st = st + 1 == S ? 0 : st + 1;
         }
     }
     fold();
