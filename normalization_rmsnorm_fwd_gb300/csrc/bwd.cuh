@@ -410,13 +410,16 @@ k_rmsnorm_bwd(const BwdParams p)
         int64_t t = r0 + grp;                // row of iteration it
         uint16_t *dxrow = p.dx + t * p.lddx + (int64_t)lane * VEC;
         int st = 0;                          // its stage
-        for (int64_t it = 0; it < iters; ++it) {
+        // One iteration; `checked` = false when rows it and it+1 are known to
+        // be live (every iteration but the last two), so the body has no
+        // liveness tests.
+        auto step = [&](int64_t it, bool checked) {
             issue_next();                    // iteration it + D
             cp_async_wait<D - 1>();          // this thread's copies of rows it, it+1 landed
             const float rs = rs_of(it, it);
             const F2 rsn2 = f2(rs_of(it + 1, it));
-            const bool live = t < r1;
-            const bool live_n = t + rpc < r1;
+            const bool live = !checked || t < r1;
+            const bool live_n = !checked || t + rpc < r1;
             const int st_n = st + 1 == S ? 0 : st + 1;
             F2 rs2, nc3;
             coefs(rs, tot, rs2, nc3);
@@ -436,7 +439,10 @@ k_rmsnorm_bwd(const BwdParams p)
             st = st_n;
             __syncthreads();
             tot = group_total(it + 1);
-        }
+        };
+        int64_t it = 0;
+        for (; it + 2 < iters; ++it) step(it, false);
+        for (; it < iters; ++it) step(it, true);
     } else {
         int64_t t = r0 + grp;                // row of iteration it
         uint16_t *dxrow = p.dx + t * p.lddx + (int64_t)lane * VEC;
