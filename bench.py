@@ -222,6 +222,17 @@ def other_kernels(dev, peak):
 
     sc = torch.tensor([0.04], device=dev)
 
+    # The backward on its own (dx + deterministic dw, both launches), not
+    # preceded by a forward whose dirty L2 lines are written back meanwhile.
+    def bwd():
+        g, x = randn(16384, 4096), randn(16384, 4096)
+        w = randn(4096, scale=0.1, shift=1.0)
+        rstd = torch.rand(16384, device=dev) + 0.5
+        dx, dw = torch.empty_like(x), torch.empty(4096, device=dev)
+        ws = crm.rmsnorm_bwd_workspace(16384, 4096, dev)
+        return lambda: crm.rmsnorm_bwd(g, x, w, rstd, dx=dx, dw=dw, workspace=ws)
+    add("rmsnorm_bwd alone T=16384 H=4096 (dx + dw, two launches)", bwd, 402_743_296)
+
     def plain():
         x, w = randn(16384, 4096), randn(4096, scale=0.1, shift=1.0)
         y, r = torch.empty_like(x), torch.empty(16384, device=dev)
