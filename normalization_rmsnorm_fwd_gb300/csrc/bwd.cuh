@@ -12,15 +12,20 @@
 // FP32 sum (one fused multiply-add per row) of its last kDwBlock rows plus a
 // compensated (TwoSum) FP32 pair into which each block sum is folded, all in
 // registers, while it walks its chunk (error <= kDwBlock ulp of the summed
-// magnitudes).  Elementwise arithmetic uses packed FP32x2 instructions.
-// Rows stream through a ring of shared-memory stages filled with cp.async:
-// every thread copies exactly the 16-byte (or 4-byte) pieces of g, x
-// (g_residual) and rstd that it will itself consume, D rows ahead, and waits
-// only on its own copy groups (cp.async.wait_group), so D rows per CTA are in
-// flight without any register cost and without any cross-thread handoff or
-// flag spinning.  At the end the CTA adds its row groups in group order and
-// writes one FP32 partial row; a second kernel (bwd_reduce.cu) adds the
-// partial rows of each column in chunk order.
+// magnitudes).  Elementwise arithmetic uses packed FP32x2 instructions, and
+// the products g*x come exact from mixed-precision BF16 FMAs.  Rows stream
+// through a ring of shared-memory stages filled with cp.async: every thread
+// copies exactly the 16-byte (or 4-byte) pieces of g and x (g_residual) that
+// it will itself consume, D rows ahead, and waits only on its own copy groups
+// (cp.async.wait_group), so D rows per CTA are in flight without any register
+// cost, cross-thread handoff or flag spinning; rstd is read 32 rows at a time
+// into registers and broadcast by shuffles.  Multi-warp rows run a software
+// pipeline (row i+1's sum formed while row i gets its dx, one CTA barrier per
+// row); the per-row integer work is kept to running pointers and counters,
+// since at about 20 instructions per element the kernel is bound by issue.
+// At the end the CTA adds its row groups in group order and writes one FP32
+// partial row; a second kernel (bwd_reduce.cu) adds the partial rows of each
+// column in a fixed order.
 #pragma once
 
 #include <atomic>
