@@ -19,8 +19,10 @@
 //   o      = (h * rstd) * f32(w + bias)
 //   then one of the epilogues below.
 // LayerNorm rows ("FlashInfer normalization operator guide" 4) take the mean
-// first and then the sum of squared deviations (both compensated across
-// threads): rstd = 1 / sqrt(ss_dev / H + eps), o = (h - mean)*rstd*gamma + beta.
+// first and then the sum of squared deviations from it (plain FP32 sums in a
+// fixed tree: the deviations' squares are all positive, and the mean's
+// absolute error stays near 2^-21 of mean|x|): rstd = 1 / sqrt(ss_dev / H +
+// eps), o = (h - mean)*rstd*gamma + beta.
 //
 // Two launch forms.  One row per group per CTA (LOOP = false): a grid of
 // ceil(T / rpc) CTAs.  Persistent (LOOP = true, the plain row with the y or
@@ -56,7 +58,7 @@ k_rmsnorm_fwd(const FwdParams p)
     constexpr bool ADA = (OUT == OUT_ADA || OUT == OUT_ADA_Q);
     constexpr bool LN = (IN == IN_LAYERNORM);
     __shared__ float red_h[32], red_l[32];
-    __shared__ float red2_h[LN ? 32 : 1], red2_l[LN ? 32 : 1];
+    __shared__ float red2_h[LN ? 32 : 1];
 
     const int tpr = p.tpr;
     const int grp = threadIdx.x / tpr;
@@ -193,9 +195,29 @@ k_rmsnorm_fwd(const FwdParams p)
             }
             return __fadd_rn(sh_, sl_);
         };
+        // The same sum in plain FP32 (a fixed butterfly, then the group's
+        // warps in a fixed tree): LayerNorm's two sums, whose accuracy needs
+        // are met without compensation.
+        auto row_sum_plain = [&](F2 part, float *rh) -> float {
+            float v = __fadd_rn(f2_lo(part), f2_hi(part));
+            const int width = SUB ? tpr : 32;
+            for (int o = width >> 1; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if constexpr (!SUB) {
+                const int nwarp = tpr >> 5;
+                const int warp = threadIdx.x >> 5;
+                if ((threadIdx.x & 31) == 0) rh[warp] = v;
+                __syncthreads();
+                int w = 1;
+                while (w < nwarp) w <<= 1;
+                const int i = threadIdx.x & (w - 1);
+                v = i < nwarp ? rh[grp * nwarp + i] : 0.f;
+                for (int o = w >> 1; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+            }
+            return v;
+        };
         float mean = 0.f;
         if constexpr (LN) {
-            mean = __fdiv_rn(row_sum(ss2, red2_h, red2_l), (float)p.H);
+            mean = __fdiv_rn(row_sum_plain(ss2, red2_h), (float)p.H);
             // Squared deviations of this thread's elements (none past the row).
             const F2 nm2 = f2(-mean);
             ss2 = f2(0.f);
@@ -211,7 +233,9 @@ k_rmsnorm_fwd(const FwdParams p)
             if (p.mean != nullptr && live && lane == 0)
                 p.mean[t] = mean;
         }
-        const float ssum = row_sum(ss2, red_h, red_l);
+        float ssum;
+        if constexpr (LN) ssum = row_sum_plain(ss2, red_h);
+        else ssum = row_sum(ss2, red_h, red_l);
         const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ssum, (float)p.H), p.eps)));
         if (p.rstd != nullptr && live && lane == 0)
             p.rstd[t] = rstd;
