@@ -131,7 +131,7 @@ k_rmsnorm_bwd(const BwdParams p)
     const int64_t iters = (r1 - r0 + rpc - 1) / rpc;
 
     // Shared memory: ring [S][stage], then w_eff [VPT*tpr*VEC] (zero past H),
-    // then the row-group combine area [rpc-1][H][2].  w_eff is stored in two
+    // then the row-group combine area [rpc][H][2] (when rpc > 1).  w_eff is stored in two
     // planes of four values per vector (one plane for VEC == 2), so that the
     // 16-byte loads of a warp touch consecutive addresses.
     const int stage_bytes = bwd_stage_bytes(NT, VPT, VEC, nthr);
@@ -493,37 +493,32 @@ k_rmsnorm_bwd(const BwdParams p)
     cp_async_wait<0>();
 
     // Combine the CTA's row groups in group order, then write the partial row.
+    // With several groups, every group stores its (sum, compensation) pairs in
+    // comb[group][column], and after one barrier each thread adds whole
+    // columns over the groups in group order (the same order, so the same
+    // bits, as one group adding the others in turn, but spread over the CTA).
+    float *prow = p.part + (int64_t)blockIdx.x * p.H;
     if (rpc > 1) {
-        if (grp > 0) {
 #pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const int v = k * tpr + lane;
-                if (v < nvec)
+        for (int k = 0; k < VPT; ++k) {
+            const int v = k * tpr + lane;
+            if (v < nvec)
 #pragma unroll
-                    for (int i = 0; i < VEC; ++i) {
-                        float *c2 = comb + ((int64_t)(grp - 1) * p.H + (int64_t)v * VEC + i) * 2;
-                        c2[0] = acc[k][i];
-                        c2[1] = cmp[k][i];
-                    }
-            }
+                for (int i = 0; i < VEC; ++i)
+                    *reinterpret_cast<float2 *>(comb + ((int64_t)grp * p.H + (int64_t)v * VEC + i) * 2) =
+                        make_float2(acc[k][i], cmp[k][i]);
         }
         __syncthreads();
-        if (grp == 0) {
-            for (int gi = 1; gi < rpc; ++gi)
-#pragma unroll
-                for (int k = 0; k < VPT; ++k) {
-                    const int v = k * tpr + lane;
-                    if (v < nvec)
-#pragma unroll
-                        for (int i = 0; i < VEC; ++i) {
-                            const float *c2 = comb + ((int64_t)(gi - 1) * p.H + (int64_t)v * VEC + i) * 2;
-                            pair_add(acc[k][i], cmp[k][i], c2[0], c2[1]);
-                        }
-                }
+        for (int col = threadIdx.x; col < p.H; col += nthr) {
+            const float2 c0 = *reinterpret_cast<const float2 *>(comb + (int64_t)col * 2);
+            float h = c0.x, l = c0.y;
+            for (int gi = 1; gi < rpc; ++gi) {
+                const float2 c = *reinterpret_cast<const float2 *>(comb + ((int64_t)gi * p.H + col) * 2);
+                pair_add(h, l, c.x, c.y);
+            }
+            prow[col] = __fadd_rn(h, l);
         }
-    }
-    if (grp == 0) {
-        float *prow = p.part + (int64_t)blockIdx.x * p.H;
+    } else {
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = k * tpr + lane;
@@ -542,7 +537,7 @@ k_rmsnorm_bwd(const BwdParams p)
 inline size_t bwd_smem_bytes(bool gres, int vec, int vpt, int threads, int rpc, int H, int D)
 {
     return (size_t)(D + 1) * bwd_stage_bytes(gres ? 3 : 2, vpt, vec, threads) +
-           ((size_t)vpt * (threads / rpc) * vec + (size_t)(rpc - 1) * H * 2) * sizeof(float);
+           ((size_t)vpt * (threads / rpc) * vec + (rpc > 1 ? (size_t)rpc * H * 2 : 0)) * sizeof(float);
 }
 
 // Launch of one instantiation: picks the chunk count from the occupancy of
