@@ -37,6 +37,12 @@
  *     overlap between an output and another tensor returns CRMSN_ERR_ALIAS.
  *   - The functions are safe to call from several host threads; kernels on
  *     one stream run in order.
+ *   - Kernels are launched with programmatic dependent launch allowed, so a
+ *     grid may be scheduled while the kernel before it in the stream is
+ *     still running; each one waits (griddepcontrol.wait) for that kernel to
+ *     complete before it touches memory.  A caller's own kernel launched
+ *     with that attribute right after one of these must wait the same way
+ *     before reading their outputs.
  */
 #ifndef CRMSNORM_H
 #define CRMSNORM_H

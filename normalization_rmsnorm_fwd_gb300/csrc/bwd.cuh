@@ -119,6 +119,11 @@ k_rmsnorm_bwd(const BwdParams p)
     // Per-warp row sums of the pipelined path: [row parity][group][warp].
     __shared__ __align__(16) float wsum[PIPE ? 2 * kBwdMaxGroups * kBwdMaxGroupWarps : 4];
     extern __shared__ __align__(16) unsigned char dyn_smem[];
+    // Programmatic dependent launch: wait for the preceding grid (and its
+    // memory) before any global access; let the reduce grid be scheduled now
+    // (it waits for this whole grid the same way).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int nthr = blockDim.x;
     const int tpr = p.tpr;
@@ -528,9 +533,6 @@ k_rmsnorm_bwd(const BwdParams p)
                     prow[(int64_t)v * VEC + i] = __fadd_rn(acc[k][i], cmp[k][i]);
         }
     }
-    // Let the dependent reduce grid get scheduled; it still waits for this
-    // whole grid (and its memory) with griddepcontrol.wait.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Dynamic shared memory of one CTA for a layout and prefetch depth D.
@@ -565,9 +567,8 @@ cudaError_t launch_bwd_inst(BwdParams p, int sms, int *nchunk_out, cudaStream_t 
     const int64_t by_rows = (p.T + p.rpc - 1) / p.rpc;
     const int64_t cap = (int64_t)per_sm * sms;
     p.nchunk = (int)(by_rows < cap ? by_rows : cap);
-    kern<<<p.nchunk, threads, smem, s>>>(p);
     *nchunk_out = p.nchunk;
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)p.nchunk), dim3(threads), smem, s, p);
 }
 
 // Dispatch over layouts (SUB groups with VPT 1|2; multi-warp groups with VPT

@@ -1,6 +1,6 @@
 // bwd_reduce.cu -- the fixed-order reduction of the backward's per-chunk dw
 // partial rows, and the backward launch sequence (partials kernel, then this
-// reduction with programmatic dependent launch).
+// reduction; every launch uses programmatic dependent launch).
 #include "launch.h"
 
 namespace crmsn {
@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(32 * kReduceWarps)
 k_dw_reduce(const float *__restrict__ part, int nchunk, int H, float *__restrict__ dw)
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ float sh_h[kReduceWarps][33], sh_l[kReduceWarps][33];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -54,25 +55,8 @@ k_dw_reduce(const float *__restrict__ part, int nchunk, int H, float *__restrict
 
 static cudaError_t launch_dw_reduce(const float *part, int nchunk, int H, float *dw, cudaStream_t s)
 {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((H + 31) / 32));
-    cfg.blockDim = dim3(32 * kReduceWarps);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k_dw_reduce, part, nchunk, H, dw);
-    if (e != cudaSuccess) {
-        // Without the attribute the launch is an ordinary stream-ordered one;
-        // griddepcontrol.wait then returns at once.
-        (void)cudaGetLastError();
-        cfg.numAttrs = 0;
-        e = cudaLaunchKernelEx(&cfg, k_dw_reduce, part, nchunk, H, dw);
-    }
-    return e;
+    return launch_pdl(k_dw_reduce, dim3((unsigned)((H + 31) / 32)), dim3(32 * kReduceWarps), 0, s,
+                      part, nchunk, H, dw);
 }
 
 cudaError_t launch_bwd(BwdParams p, bool w32, bool gres, const Layout &L, int sms, float *dw,

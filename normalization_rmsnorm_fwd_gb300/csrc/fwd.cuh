@@ -59,6 +59,11 @@ k_rmsnorm_fwd(const FwdParams p)
     constexpr bool LN = (IN == IN_LAYERNORM);
     __shared__ float red_h[32], red_l[32];
     __shared__ float red2_h[LN ? 32 : 1];
+    // Programmatic dependent launch: wait for the preceding grid (and its
+    // memory) before any global access; let the next grid be scheduled now
+    // (it waits for this whole grid the same way).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int tpr = p.tpr;
     const int grp = threadIdx.x / tpr;
@@ -419,8 +424,7 @@ cudaError_t launch_fwd_inst(const FwdParams &p, cudaStream_t s)
         const int64_t cap = (int64_t)per_sm * sms;
         if (blocks > cap) blocks = cap;
     }
-    kern<<<(unsigned)blocks, threads, 0, s>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3((unsigned)blocks), dim3(threads), 0, s, p);
 }
 
 // Dispatch over the row layouts the host chooser can return: SUB groups with

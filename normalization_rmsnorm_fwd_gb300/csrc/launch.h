@@ -71,6 +71,37 @@ struct Layout {
 };
 
 // Forward launches, one per epilogue family (fwd_*.cu).
+// Launches kern<<<grid, block, smem, s>>>(args...) with programmatic
+// dependent launch allowed: the grid may be scheduled while the kernel before
+// it in the stream is still running.  Every kernel of this library that is
+// launched this way executes griddepcontrol.wait before its first access to
+// global memory, which returns once the preceding grid has completed and its
+// writes are visible, so stream order is kept.  Where the attribute is
+// refused the launch is an ordinary stream-ordered one (the wait then
+// returns at once).
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        cfg.numAttrs = 0;
+        e = cudaLaunchKernelEx(&cfg, kern, args...);
+    }
+    return e;
+}
+
 cudaError_t launch_fwd_y(const FwdParams &p, int in, bool w32, const Layout &L, cudaStream_t s);
 cudaError_t launch_fwd_q(const FwdParams &p, int in, bool w32, int fp8k, const Layout &L, cudaStream_t s);
 cudaError_t launch_fwd_block(const FwdParams &p, const Layout &L, cudaStream_t s);
