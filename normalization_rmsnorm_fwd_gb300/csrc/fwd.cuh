@@ -38,21 +38,49 @@
 
 namespace crmsn {
 
-// SiLU(v) = v / (1 + exp(-v)) as v * sigmoid(v) with e = exp(-|v|) in (0, 1]
-// (no overflow for any finite v): sigmoid = 1 / (1 + e) for v >= 0 and
-// e / (1 + e) otherwise.  __expf and the approximate reciprocal of 1 + e (in
-// [1, 2]) keep the relative error near 2^-20 for |v| < 10 and far below a
-// BF16 half-ulp everywhere.
-__device__ __forceinline__ float silu_f32(float v)
+// SiLU of a pair, v / (1 + exp(-v)), as v * RCP(1 + 2^(-v * log2 e)): the
+// products and the sum packed, the base-2 exponential and the reciprocal
+// from the approximate hardware instructions (ex2.approx, __fdividef).  The
+// relative error stays near 2^-20 (most of it from rounding v * log2 e, up
+// to |v| * 2^-24) -- far below a BF16 half-ulp.  Extremes: for v > ~88 the
+// exponential flushes to 0 and the result is v; for v < ~-87 it exceeds
+// 2^126, the reciprocal flushes to 0 and the result is -0 (|SiLU(v)| is
+// below 1e-35 there); +-inf and NaN give what v * sigmoid(v) gives.
+// Four (two) FP32 values to / from 16-byte (8-byte) aligned shared memory.
+// Plain loads, which the compiler may schedule early (measured: faster than
+// keeping them in program order with the epilogue's stores).
+__device__ __forceinline__ void ld_smem_f32x4(const float *p, float *f)
 {
-    const float e = __expf(-fabsf(v));
-    const float r = __fdividef(1.0f, 1.0f + e);
-    return v * (v >= 0.f ? r : e * r);
+    const float4 v = *reinterpret_cast<const float4 *>(p);
+    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+}
+__device__ __forceinline__ void ld_smem_f32x2(const float *p, float *f)
+{
+    const float2 v = *reinterpret_cast<const float2 *>(p);
+    f[0] = v.x; f[1] = v.y;
+}
+__device__ __forceinline__ void st_smem_f32x4(float *p, const float *f)
+{
+    *reinterpret_cast<float4 *>(p) = make_float4(f[0], f[1], f[2], f[3]);
 }
 
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ F2 silu_f2(F2 v)
+{
+    const F2 t = f2_mul(v, f2(-1.4426950408889634f));      // -v * log2(e)
+    const F2 d = f2_add(f2(ex2_approx(f2_lo(t)), ex2_approx(f2_hi(t))), f2(1.f));
+    return f2_mul(v, f2(__fdividef(1.0f, f2_lo(d)), __fdividef(1.0f, f2_hi(d))));
+}
+
+// The kernel body.
 template <int IN, bool W32, int OUT, int FP8K, int VEC, int VPT, bool SUB, bool LOOP>
-__global__ void __launch_bounds__(kFwdMaxThreads)
-k_rmsnorm_fwd(const FwdParams p)
+__device__ __forceinline__ void fwd_body(const FwdParams &p)
 {
     constexpr int NW = VEC / 2;
     constexpr bool ADA = (OUT == OUT_ADA || OUT == OUT_ADA_Q);
@@ -71,14 +99,21 @@ k_rmsnorm_fwd(const FwdParams p)
     const int nvec = p.H / VEC;
 
     // ---------------- phase 1: loads ---------------------------------------
-    // Weights (and LayerNorm's beta): row-independent.  LayerNorm loads gamma
-    // and beta in its epilogue instead, vector by vector, so that they do not
-    // hold registers through the two reductions.
-    constexpr bool LN_LATE = LN;
+    // Weights: row-independent, in registers.  LayerNorm's gamma and beta do
+    // not stay in registers through its two reductions: the persistent form
+    // keeps them in shared memory (loaded once per CTA), the one-row form
+    // loads them in its epilogue, vector by vector.
+    constexpr bool LN_SMEM = LN && LOOP;
+    constexpr bool LN_LATE = LN && !LOOP;
+    // LN_SMEM: gamma then beta, 2H floats; for 16-byte vectors each stored as
+    // two planes (the first and the last four values of every vector), so
+    // that a warp's 16-byte reads of consecutive vectors hit distinct banks.
+    extern __shared__ __align__(16) unsigned char fwd_dyn_smem[];
+    float *const ln_gb = reinterpret_cast<float *>(fwd_dyn_smem);
     BVec<VEC> wb[VPT];
     float wf[VPT][VEC], bt[VPT][VEC];
     auto load_weight_vec = [&](int k) {
-        if constexpr (LN_LATE) return;
+        if constexpr (LN) return;
         const int v = k * tpr + lane;
         if (v < nvec) {
             const int64_t c = (int64_t)v * VEC;
@@ -220,9 +255,25 @@ k_rmsnorm_fwd(const FwdParams p)
             }
             return v;
         };
+        // The row's FP32 values are unpacked again from the BF16 words after
+        // each reduction instead of being kept (twice the registers) across
+        // it: the empty asm makes the words opaque to the compiler.  Measured
+        // per variant: it pays where the epilogue is long (SiLU, block
+        // quantisation, one-row LayerNorm) and in the persistent y form.
+        constexpr bool REUNPACK = (LN && !LOOP) || OUT == OUT_SILU || OUT == OUT_SILU_Q ||
+                                  OUT == OUT_BLOCK || (LOOP && OUT == OUT_Y && !LN);
+        auto reunpack = [&]() {
+            if constexpr (REUNPACK) {
+#pragma unroll
+                for (int k = 0; k < VPT; ++k)
+#pragma unroll
+                    for (int i = 0; i < NW; ++i) asm volatile("" : "+r"(h[k].w[i]));
+            }
+        };
         float mean = 0.f;
         if constexpr (LN) {
             mean = __fdiv_rn(row_sum_plain(ss2, red2_h), (float)p.H);
+            reunpack();
             // Squared deviations of this thread's elements (none past the row).
             const F2 nm2 = f2(-mean);
             ss2 = f2(0.f);
@@ -241,6 +292,7 @@ k_rmsnorm_fwd(const FwdParams p)
         float ssum;
         if constexpr (LN) ssum = row_sum_plain(ss2, red_h);
         else ssum = row_sum(ss2, red_h, red_l);
+        reunpack();
         const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ssum, (float)p.H), p.eps)));
         if (p.rstd != nullptr && live && lane == 0)
             p.rstd[t] = rstd;
@@ -261,6 +313,23 @@ k_rmsnorm_fwd(const FwdParams p)
             const int v = k * tpr + lane;
             const bool ok = live && v < nvec;
             const int64_t c = (int64_t)v * VEC;
+            if constexpr (LN_SMEM) {
+                if (v < nvec) {
+                    if constexpr (VEC == 8) {
+                        const int hp = p.H >> 1;
+                        ld_smem_f32x4(ln_gb + v * 4, wf[k]);
+                        ld_smem_f32x4(ln_gb + hp + v * 4, wf[k] + 4);
+                        ld_smem_f32x4(ln_gb + p.H + v * 4, bt[k]);
+                        ld_smem_f32x4(ln_gb + p.H + hp + v * 4, bt[k] + 4);
+                    } else {
+                        ld_smem_f32x2(ln_gb + c, wf[k]);
+                        ld_smem_f32x2(ln_gb + p.H + c, bt[k]);
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < VEC; ++i) { wf[k][i] = 0.f; bt[k][i] = 0.f; }
+                }
+            }
             if constexpr (LN_LATE) {
                 if (v < nvec) {
                     ld_f32_keep<VEC>(static_cast<const float *>(p.w) + c, wf[k]);
@@ -330,19 +399,22 @@ k_rmsnorm_fwd(const FwdParams p)
             } else if constexpr (OUT == OUT_SILU) {
                 BVec<VEC> yv;
 #pragma unroll
-                for (int i = 0; i < NW; ++i) yv.w[i] = pack_bf16(silu_f32(f2_lo(o[i])), silu_f32(f2_hi(o[i])));
+                for (int i = 0; i < NW; ++i) yv.w[i] = bf16_f2(silu_f2(o[i]));
                 if (ok) st_stream<VEC>(p.y + t * p.ldy + c, yv);
             } else if constexpr (OUT == OUT_SILU_Q) {
                 uint32_t cq[NW];
                 if (p.scale == nullptr) {      // the plain cast (no division by 1)
 #pragma unroll
-                    for (int i = 0; i < NW; ++i)
-                        cq[i] = pack_fp8<0>(silu_f32(f2_lo(o[i])), silu_f32(f2_hi(o[i])));
+                    for (int i = 0; i < NW; ++i) {
+                        const F2 y2 = silu_f2(o[i]);
+                        cq[i] = pack_fp8<0>(f2_lo(y2), f2_hi(y2));
+                    }
                 } else {
 #pragma unroll
-                    for (int i = 0; i < NW; ++i)
-                        cq[i] = pack_fp8<0>(__fdiv_rn(silu_f32(f2_lo(o[i])), scale_v),
-                                            __fdiv_rn(silu_f32(f2_hi(o[i])), scale_v));
+                    for (int i = 0; i < NW; ++i) {
+                        const F2 y2 = silu_f2(o[i]);
+                        cq[i] = pack_fp8<0>(__fdiv_rn(f2_lo(y2), scale_v), __fdiv_rn(f2_hi(y2), scale_v));
+                    }
                 }
                 if (ok) st_fp8<VEC>(p.q + t * p.ldq + c, cq);
             } else {  // ADA: o * (1 + scale) + shift, one FP32 rounding (fma)
@@ -376,46 +448,104 @@ k_rmsnorm_fwd(const FwdParams p)
         load_row(t, xa, true);
         process(t);
     } else {
-        static_assert(IN == IN_PLAIN, "the persistent form streams one input");
+        static_assert(IN == IN_PLAIN || LN, "the persistent form streams one input");
         load_weights();
         const int64_t stride = (int64_t)gridDim.x * p.rpc;
         const int64_t b0 = (int64_t)blockIdx.x * p.rpc;
         load_row(b0 + grp, xa, false);
+        if constexpr (LN_SMEM) {
+            // gamma and beta into shared memory, the whole CTA striding over
+            // the vectors (the first row's loads are already in flight).
+            const float *gam = static_cast<const float *>(p.w);
+            for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+                float g[VEC], b[VEC];
+                ld_f32_keep<VEC>(gam + (int64_t)v * VEC, g);
+                ld_f32_keep<VEC>(p.beta + (int64_t)v * VEC, b);
+                if constexpr (VEC == 8) {
+                    const int hp = p.H >> 1;
+                    st_smem_f32x4(ln_gb + v * 4, g);
+                    st_smem_f32x4(ln_gb + hp + v * 4, g + 4);
+                    st_smem_f32x4(ln_gb + p.H + v * 4, b);
+                    st_smem_f32x4(ln_gb + p.H + hp + v * 4, b + 4);
+                } else {
+                    *reinterpret_cast<float2 *>(ln_gb + v * 2) = make_float2(g[0], g[1]);
+                    *reinterpret_cast<float2 *>(ln_gb + p.H + v * 2) = make_float2(b[0], b[1]);
+                }
+            }
+            __syncthreads();
+        }
+        // The next row: loaded into registers before this row is processed
+        // (PF == 2), or only prefetched into L2 then and loaded afterwards
+        // (PF == 1: no registers held across the row).
+        constexpr int PF = (LN || OUT == OUT_Q) ? 2 : 1;
         for (int64_t base = b0; base < p.T; base += stride) {
             BVec<VEC> xn[VPT];
             const bool more = base + stride < p.T;   // the same for the whole CTA
-            if (more) load_row(base + stride + grp, xn, false);
+            const int64_t tn = base + stride + grp;
+            if (more) {
+                if constexpr (PF == 2) {
+                    load_row(tn, xn, false);
+                } else if (tn < p.T) {
+#pragma unroll
+                    for (int k = 0; k < VPT; ++k) {
+                        const int v = k * tpr + lane;
+                        if (v < nvec)
+                            asm volatile("prefetch.global.L2 [%0];" :: "l"(p.x + tn * p.ldx + (int64_t)v * VEC));
+                    }
+                }
+            }
             process(base + grp);
             if (more) {
+                if constexpr (PF == 2) {
 #pragma unroll
-                for (int k = 0; k < VPT; ++k) xa[k] = xn[k];
+                    for (int k = 0; k < VPT; ++k) xa[k] = xn[k];
+                } else {
+                    load_row(tn, xa, false);
+                }
             }
         }
     }
 }
 
-// Host-side launch of one instantiation.  The single-input variants run the
-// persistent form on at most (resident CTAs per SM) x (SMs) CTAs; the
-// residency of a block size is computed once and remembered.
-template <int IN, bool W32, int OUT, int FP8K, int VEC, int VPT, bool SUB>
-cudaError_t launch_fwd_inst(const FwdParams &p, cudaStream_t s)
+// No minimum CTA count in the launch bounds: an explicit one (even 1) lets
+// the compiler take far more registers for these kernels.
+template <int IN, bool W32, int OUT, int FP8K, int VEC, int VPT, bool SUB, bool LOOP>
+__global__ void __launch_bounds__(kFwdMaxThreads) k_rmsnorm_fwd(const FwdParams p)
 {
-    // Measured: the persistent form pays off for the plain row with the y and
-    // static FP8 epilogues; SiLU (bound by its arithmetic) and LayerNorm
-    // (gamma and beta) run faster in the one-row form.
-    constexpr bool LOOP = IN == IN_PLAIN && (OUT == OUT_Y || OUT == OUT_Q);
+    fwd_body<IN, W32, OUT, FP8K, VEC, VPT, SUB, LOOP>(p);
+}
+
+// Host-side launch of one kernel.  The persistent form runs on at most
+// (resident CTAs per SM) x (SMs) CTAs; the residency for a block size and
+// shared-memory size is computed once and remembered.
+template <int IN, bool W32, int OUT, int FP8K, int VEC, int VPT, bool SUB, bool LOOP>
+cudaError_t launch_fwd_kernel(const FwdParams &p, size_t smem, cudaStream_t s)
+{
     auto kern = k_rmsnorm_fwd<IN, W32, OUT, FP8K, VEC, VPT, SUB, LOOP>;
     const int threads = p.tpr * p.rpc;
     int64_t blocks = (p.T + p.rpc - 1) / p.rpc;
-    if constexpr (LOOP) {
-        static std::atomic<long long> cached{0};   // threads << 32 | CTAs per SM
-        long long c = cached.load(std::memory_order_relaxed);
-        int per_sm = (int)(c & 0xffffffff);
-        if ((c >> 32) != threads || per_sm <= 0) {
-            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0);
+    if (smem > 48 * 1024) {
+        // Opt in to more than the default dynamic shared memory (the largest
+        // size requested so far is remembered).
+        static std::atomic<long long> opted{0};
+        if ((long long)smem > opted.load(std::memory_order_relaxed)) {
+            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
-            if (per_sm < 1) per_sm = 1;
-            cached.store(((long long)threads << 32) | per_sm, std::memory_order_relaxed);
+            opted.store((long long)smem, std::memory_order_relaxed);
+        }
+    }
+    if constexpr (LOOP) {
+        // threads << 40 | shared-memory bytes << 8 | CTAs per SM
+        static std::atomic<long long> cached{0};
+        const long long key = ((long long)threads << 40) | ((long long)smem << 8);
+        long long c = cached.load(std::memory_order_relaxed);
+        int per_sm = (int)(c & 0xff);
+        if ((c & ~0xffLL) != key || per_sm <= 0) {
+            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+            if (e != cudaSuccess) return e;
+            if (per_sm < 1) return cudaErrorInvalidConfiguration;
+            if (per_sm > 255) per_sm = 255;
+            cached.store(key | per_sm, std::memory_order_relaxed);
         }
         int dev = 0, sms = 0;
         cudaError_t e = cudaGetDevice(&dev);
@@ -424,7 +554,29 @@ cudaError_t launch_fwd_inst(const FwdParams &p, cudaStream_t s)
         const int64_t cap = (int64_t)per_sm * sms;
         if (blocks > cap) blocks = cap;
     }
-    return launch_pdl(kern, dim3((unsigned)blocks), dim3(threads), 0, s, p);
+    return launch_pdl(kern, dim3((unsigned)blocks), dim3(threads), smem, s, p);
+}
+
+// LayerNorm keeps gamma and beta (2H floats) in shared memory in the
+// persistent form up to this size; wider rows use the one-row form.
+constexpr size_t kLnSmemMax = 64 * 1024;
+
+// Launch of one instantiation.  Measured: the persistent form pays off for
+// the plain row with the y and static FP8 epilogues and for LayerNorm with
+// gamma and beta in shared memory; SiLU (bound by its arithmetic) runs
+// faster in the one-row form.
+template <int IN, bool W32, int OUT, int FP8K, int VEC, int VPT, bool SUB>
+cudaError_t launch_fwd_inst(const FwdParams &p, cudaStream_t s)
+{
+    if constexpr (IN == IN_LAYERNORM) {
+        const size_t smem = (size_t)2 * p.H * sizeof(float);
+        if (smem <= kLnSmemMax)
+            return launch_fwd_kernel<IN, W32, OUT, FP8K, VEC, VPT, SUB, true>(p, smem, s);
+        return launch_fwd_kernel<IN, W32, OUT, FP8K, VEC, VPT, SUB, false>(p, 0, s);
+    } else {
+        constexpr bool LOOP = IN == IN_PLAIN && (OUT == OUT_Y || OUT == OUT_Q);
+        return launch_fwd_kernel<IN, W32, OUT, FP8K, VEC, VPT, SUB, LOOP>(p, 0, s);
+    }
 }
 
 // Dispatch over the row layouts the host chooser can return: SUB groups with
