@@ -137,6 +137,25 @@ struct DivScale {
             hi = __fdiv_rn(f2_hi(v), s);
         }
     }
+    // n pairs at once, the choice between the two forms taken once.
+    template <int N>
+    __device__ __forceinline__ void div_n(const F2 (&v)[N], float (&lo)[N], float (&hi)[N]) const
+    {
+        if (fast) {
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                const F2 q = f2_div_recip(v[i], s, r);
+                lo[i] = f2_lo(q);
+                hi[i] = f2_hi(q);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                lo[i] = __fdiv_rn(f2_lo(v[i]), s);
+                hi[i] = __fdiv_rn(f2_hi(v[i]), s);
+            }
+        }
+    }
 };
 // FP32 pair -> packed BF16 pair, round to nearest even.
 __device__ __forceinline__ uint32_t bf16_f2(F2 a) { return pack_bf16(f2_lo(a), f2_hi(a)); }
