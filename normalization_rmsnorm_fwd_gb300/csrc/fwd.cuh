@@ -85,6 +85,10 @@ __device__ __forceinline__ F2 silu_f2(F2 v)
     return f2_mul(v, f2(rcp_approx(f2_lo(d)), rcp_approx(f2_hi(d))));
 }
 
+// How the persistent form fetches the next row ahead: 1 = prefetched into
+// L2, 2 = loaded into registers (measured per epilogue).
+constexpr int fwd_prefetch(int in, int out) { return in == IN_LAYERNORM || out == OUT_Q ? 2 : 1; }
+
 // The kernel body.
 template <int IN, bool W32, int OUT, int FP8K, int VEC, int VPT, bool SUB, bool LOOP>
 __device__ __forceinline__ void fwd_body(const FwdParams &p)
@@ -457,6 +461,7 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
         load_weights();
         const int64_t stride = (int64_t)gridDim.x * p.rpc;
         const int64_t b0 = (int64_t)blockIdx.x * p.rpc;
+        constexpr int PF = fwd_prefetch(IN, OUT);
         load_row(b0 + grp, xa, false);
         if constexpr (LN_SMEM) {
             // gamma and beta into shared memory, the whole CTA striding over
@@ -479,10 +484,9 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
             }
             __syncthreads();
         }
-        // The next row: loaded into registers before this row is processed
+        // The next row is loaded into registers before this row is processed
         // (PF == 2), or only prefetched into L2 then and loaded afterwards
         // (PF == 1: no registers held across the row).
-        constexpr int PF = (LN || OUT == OUT_Q) ? 2 : 1;
         for (int64_t base = b0; base < p.T; base += stride) {
             BVec<VEC> xn[VPT];
             const bool more = base + stride < p.T;   // the same for the whole CTA
@@ -529,9 +533,10 @@ cudaError_t launch_fwd_kernel(const FwdParams &p, size_t smem, cudaStream_t s)
     auto kern = k_rmsnorm_fwd<IN, W32, OUT, FP8K, VEC, VPT, SUB, LOOP>;
     const int threads = p.tpr * p.rpc;
     int64_t blocks = (p.T + p.rpc - 1) / p.rpc;
-    if (smem > 48 * 1024) {
-        // Opt in to more than the default dynamic shared memory (the largest
-        // size requested so far is remembered).
+    if (smem > 0) {
+        // Opt in to dynamic shared memory beyond the default (which, with the
+        // kernel's static shared memory, must stay within 48 KB); the largest
+        // size requested so far is remembered.
         static std::atomic<long long> opted{0};
         if ((long long)smem > opted.load(std::memory_order_relaxed)) {
             cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -574,9 +579,9 @@ template <int IN, bool W32, int OUT, int FP8K, int VEC, int VPT, bool SUB>
 cudaError_t launch_fwd_inst(const FwdParams &p, cudaStream_t s)
 {
     if constexpr (IN == IN_LAYERNORM) {
-        const size_t smem = (size_t)2 * p.H * sizeof(float);
-        if (smem <= kLnSmemMax)
-            return launch_fwd_kernel<IN, W32, OUT, FP8K, VEC, VPT, SUB, true>(p, smem, s);
+        const size_t table = (size_t)2 * p.H * sizeof(float);
+        if (table <= kLnSmemMax)
+            return launch_fwd_kernel<IN, W32, OUT, FP8K, VEC, VPT, SUB, true>(p, table, s);
         return launch_fwd_kernel<IN, W32, OUT, FP8K, VEC, VPT, SUB, false>(p, 0, s);
     } else {
         constexpr bool LOOP = IN == IN_PLAIN && (OUT == OUT_Y || OUT == OUT_Q);

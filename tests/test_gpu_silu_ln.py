@@ -149,7 +149,9 @@ def _check_ln(orc, x, gamma, beta, eps=1e-5, rows=None, kinds=(0, 1)):
                      allowance=allow / float(np.float32(0.04)))
 
 
-@pytest.mark.parametrize("H", [2, 64, 160, 256, 1000, 2048, 3072, 4096, 5120, 8192, 16384])
+# 6144: the persistent form's gamma/beta table is exactly 48 KB, which with
+# the kernel's static shared memory needs the opt-in above the default.
+@pytest.mark.parametrize("H", [2, 64, 160, 256, 1000, 2048, 3072, 4096, 5120, 6144, 8192, 8200, 16384])
 def test_layernorm_widths(orc, H):
     x = synth.random_rows(H + 2, 45, H)[0]
     g, b = _gamma_beta(H, H)
