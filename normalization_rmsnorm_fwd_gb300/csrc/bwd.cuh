@@ -601,8 +601,8 @@ cudaError_t launch_bwd_vd(const BwdParams &p, const Layout &L, int sms, int *nc,
 constexpr size_t kBwdSmemBudget = 200 * 1024;
 
 // Prefetch depth: 3 rows ahead when four stages fit the shared-memory
-// budget, else 1, else none (only rows of 32 elements per thread at H close
-// to the maximum).
+// budget, else 2, else 1, else none (only rows of 32 elements per thread at
+// H close to the maximum).
 template <bool W32>
 cudaError_t launch_bwd_weight(const BwdParams &p, bool gres, const Layout &L, int sms, int *nc,
                               cudaStream_t s)
@@ -611,20 +611,24 @@ cudaError_t launch_bwd_weight(const BwdParams &p, bool gres, const Layout &L, in
     auto fits = [&](int d) {
         return bwd_smem_bytes(gres, L.vec, L.vpt, threads, p.rpc, p.H, d) <= kBwdSmemBudget;
     };
-    const int D = fits(3) ? 3 : (fits(1) ? 1 : 0);
+    const int D = fits(3) ? 3 : (fits(2) ? 2 : (fits(1) ? 1 : 0));
     if (L.vec == 8) {
         if (gres) return D == 3 ? launch_bwd_vd<W32, true, 8, 3>(p, L, sms, nc, s)
+                       : D == 2 ? launch_bwd_vd<W32, true, 8, 2>(p, L, sms, nc, s)
                        : D == 1 ? launch_bwd_vd<W32, true, 8, 1>(p, L, sms, nc, s)
                                 : launch_bwd_vd<W32, true, 8, 0>(p, L, sms, nc, s);
         return D == 3 ? launch_bwd_vd<W32, false, 8, 3>(p, L, sms, nc, s)
+             : D == 2 ? launch_bwd_vd<W32, false, 8, 2>(p, L, sms, nc, s)
              : D == 1 ? launch_bwd_vd<W32, false, 8, 1>(p, L, sms, nc, s)
                       : launch_bwd_vd<W32, false, 8, 0>(p, L, sms, nc, s);
     }
     if (L.vec == 2) {
         if (gres) return D == 3 ? launch_bwd_vd<W32, true, 2, 3>(p, L, sms, nc, s)
+                       : D == 2 ? launch_bwd_vd<W32, true, 2, 2>(p, L, sms, nc, s)
                        : D == 1 ? launch_bwd_vd<W32, true, 2, 1>(p, L, sms, nc, s)
                                 : launch_bwd_vd<W32, true, 2, 0>(p, L, sms, nc, s);
         return D == 3 ? launch_bwd_vd<W32, false, 2, 3>(p, L, sms, nc, s)
+             : D == 2 ? launch_bwd_vd<W32, false, 2, 2>(p, L, sms, nc, s)
              : D == 1 ? launch_bwd_vd<W32, false, 2, 1>(p, L, sms, nc, s)
                       : launch_bwd_vd<W32, false, 2, 0>(p, L, sms, nc, s);
     }

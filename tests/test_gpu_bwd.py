@@ -49,8 +49,10 @@ def test_plain_small_config(orc):
     compare(orc, d["g"], d["x"], d["w"], d["eps"])
 
 
+# 8192 with g_residual, 9002 with g_residual (4-byte path) and 12288 run the
+# backward with two rows in flight (three ring stages fit, four do not).
 @pytest.mark.parametrize("H", [2, 8, 64, 128, 200, 256, 520, 1024, 2048, 3072, 4096, 5120,
-                               6144, 8192, 16384])
+                               6144, 8192, 9002, 12288, 16384])
 @pytest.mark.parametrize("route", ["bf16", "f32", "bf16_gres"])
 def test_widths_and_routes(orc, H, route):
     T = 300
