@@ -69,6 +69,8 @@ def library_path() -> str:
 def load(path: str | None = None) -> ctypes.CDLL:
     """Load (once) and return the CUDA library; raise if it was never built."""
     global _lib
+    if path is None and _lib is not None:
+        return _lib
     with _lock:
         if _lib is None or path is not None:
             p = path or _LIB

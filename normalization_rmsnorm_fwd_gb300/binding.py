@@ -15,6 +15,7 @@ Parameters/x); any other layout raises ``ValueError``.
 """
 from __future__ import annotations
 
+import contextlib
 import math
 
 import torch
@@ -29,8 +30,26 @@ def _lib():
     return _abi.load()
 
 
+# The raw handle of the current stream without building a Stream object
+# (a few microseconds a call); the public query where it is missing.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(t: torch.Tensor) -> int:
+    if _raw_stream is not None:
+        return _raw_stream(t.get_device())
     return torch.cuda.current_stream(t.device).cuda_stream
+
+
+_SAME_DEVICE = contextlib.nullcontext()
+
+
+def _on_device(t: torch.Tensor):
+    """A context making t's device current; nothing to do when it already is."""
+    idx = t.get_device()
+    if idx == torch.cuda.current_device():
+        return _SAME_DEVICE
+    return torch.cuda.device(idx)
 
 
 def _ptr(t):
@@ -44,20 +63,23 @@ def _need_cuda(t: torch.Tensor, name: str):
 
 def as_rows(t: torch.Tensor, name: str = "x") -> tuple[int, int, int]:
     """(rows, H, row stride in elements) of a row-collapsible tensor."""
-    if t.dim() < 1:
+    shape = t.shape
+    nd = len(shape)
+    if nd < 1:
         raise ValueError(f"{name}: needs at least one dimension")
-    H = t.shape[-1]
-    if H > 1 and t.stride(-1) != 1:
+    st = t.stride()
+    H = shape[-1]
+    if H > 1 and st[-1] != 1:
         raise ValueError(f"{name}: the feature dimension must be contiguous")
-    if t.dim() == 1:
+    if nd == 1:
         return 1, H, H
-    for i in range(t.dim() - 2):
-        if t.shape[i] > 1 and t.stride(i) != t.stride(i + 1) * t.shape[i + 1]:
+    for i in range(nd - 2):
+        if shape[i] > 1 and st[i] != st[i + 1] * shape[i + 1]:
             raise ValueError(
                 f"{name}: leading dimensions must be contiguous with one another "
                 "(stride(i) == stride(i+1) * size(i+1)) to collapse into rows")
-    rows = math.prod(t.shape[:-1])
-    ld = t.stride(-2) if t.shape[-2] > 1 else max(H, t.stride(-2))
+    rows = shape[0] if nd == 2 else math.prod(shape[:-1])
+    ld = st[-2] if shape[-2] > 1 else max(H, st[-2])
     return rows, H, ld
 
 
@@ -110,7 +132,7 @@ def rmsnorm_fwd(x, w, eps: float = 1e-6, residual=None, weight_bias: float = 0.0
         rstd = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
     _, _, ldy = as_rows(y, "y")
     ldh = as_rows(h_new, "h_new")[2] if h_new is not None else 0
-    with torch.cuda.device(x.device):
+    with _on_device(x):
         st = _lib().rmsnorm_fwd(_ptr(x), ldx, _ptr(residual), ldr, _ptr(w), kind,
                                 float(weight_bias), float(eps), T, H, _ptr(y), ldy, _ptr(rstd),
                                 _ptr(h_new), ldh, _stream(x))
@@ -139,7 +161,7 @@ def fused_add_rmsnorm_quant(out, x, residual, w, scale, eps: float = 1e-6,
         _, _, ldr = as_rows(residual, "residual")
     _, _, ldo = as_rows(out, "out")
     s = _scale_tensor(scale, x.device)
-    with torch.cuda.device(x.device):
+    with _on_device(x):
         st = _lib().fused_add_rmsnorm_quant(_ptr(out), ldo, _FP8[out.dtype], _ptr(x), ldx,
                                             _ptr(residual), ldr, _ptr(w), kind,
                                             float(weight_bias), _ptr(s), float(eps), T, H,
@@ -169,7 +191,7 @@ def fused_add_rmsnorm_fp8_block_quant(out, block_scale, normed_out, x, residual,
     if block_scale.dim() != 2 or block_scale.shape[0] != H // 128:
         raise ValueError("block_scale must be (H/128, ldT)")
     ldT = block_scale.shape[1]
-    with torch.cuda.device(x.device):
+    with _on_device(x):
         st = _lib().fused_add_rmsnorm_fp8_block_quant(_ptr(out), _ptr(block_scale), ldT,
                                                       _ptr(normed_out), _ptr(x), ldx,
                                                       _ptr(residual), ldr, _ptr(w), float(eps),
@@ -192,7 +214,7 @@ def ada_rms_norm_style(x, w, style, eps: float = 1e-6, out=None, gate_out=None):
         out = torch.empty_like(x)
     if gate_out is None:
         gate_out = torch.empty_like(x)
-    with torch.cuda.device(x.device):
+    with _on_device(x):
         st = _lib().ada_rms_norm_style(_ptr(x), _ptr(w), _ptr(style), style.shape[0],
                                        float(eps), T, D, _ptr(out), _ptr(gate_out), _stream(x))
     check("ada_rms_norm_style", st)
@@ -216,7 +238,7 @@ def gate_residual_ada_norm_fp8(residual, x, gate, w, style, scale, eps: float = 
     if gate_out is None:
         gate_out = torch.empty_like(x)
     s = _scale_tensor(scale, x.device)
-    with torch.cuda.device(x.device):
+    with _on_device(x):
         st = _lib().gate_residual_ada_norm_fp8(_ptr(residual), _ptr(x), _ptr(gate), _ptr(w),
                                                _ptr(style), style.shape[0], _ptr(s),
                                                float(eps), T, D, _ptr(out), _ptr(gate_out),
@@ -245,7 +267,7 @@ def fused_rmsnorm_silu(x, w, eps: float = 1e-6, weight_bias: float = 0.0, out=No
         raise TypeError("out must be bfloat16 or float8_e4m3fn")
     _, _, ldo = as_rows(out, "out")
     s = _scale_tensor(scale, x.device) if (scale is not None and fmt == _abi.OUT_E4M3) else None
-    with torch.cuda.device(x.device):
+    with _on_device(x):
         st = _lib().fused_rmsnorm_silu(_ptr(out), ldo, fmt, _ptr(x), ldx, _ptr(w), kind,
                                        float(weight_bias), _ptr(s), float(eps), T, H,
                                        _ptr(rstd), _stream(x))
@@ -270,7 +292,7 @@ def layernorm(x, gamma, beta, eps: float = 1e-5, out=None, mean=None, rstd=None)
         out = torch.empty(x.shape, dtype=torch.bfloat16, device=x.device)
     _bf16(out, "out")
     _, _, ldo = as_rows(out, "out")
-    with torch.cuda.device(x.device):
+    with _on_device(x):
         st = _lib().layernorm(_ptr(out), ldo, _ptr(x), ldx, _ptr(gamma), _ptr(beta), float(eps),
                               T, H, _ptr(mean), _ptr(rstd), _stream(x))
     check("layernorm", st)
@@ -286,7 +308,7 @@ def layernorm_quant(out, x, gamma, beta, scale, eps: float = 1e-5, mean=None, rs
         raise TypeError("out must be float8_e4m3fn or float8_e5m2")
     _, _, ldo = as_rows(out, "out")
     s = _scale_tensor(scale, x.device)
-    with torch.cuda.device(x.device):
+    with _on_device(x):
         st = _lib().layernorm_quant(_ptr(out), ldo, _FP8[out.dtype], _ptr(x), ldx, _ptr(gamma),
                                     _ptr(beta), _ptr(s), float(eps), T, H, _ptr(mean), _ptr(rstd),
                                     _stream(x))
@@ -337,7 +359,7 @@ def rmsnorm_bwd(g, x, w, rstd, weight_bias: float = 0.0, g_residual=None, worksp
     if workspace is None:
         workspace = torch.empty(rmsnorm_bwd_workspace_bytes(T, H, x.device), dtype=torch.uint8,
                                 device=x.device)
-    with torch.cuda.device(x.device):
+    with _on_device(x):
         st = _lib().rmsnorm_bwd(_ptr(g), ldg, _ptr(x), ldx, _ptr(w), kind, float(weight_bias),
                                 _ptr(rstd), _ptr(g_residual), ldgr, T, H, _ptr(dx), lddx,
                                 _ptr(dw), _ptr(workspace), workspace.numel() * workspace.element_size(),
@@ -365,7 +387,7 @@ def rmsnorm_bwd_noalloc(g, x, w, rstd, weight_bias: float = 0.0, g_residual=None
     _, _, lddx = as_rows(dx, "dx")
     if dw is None:
         dw = torch.empty(H, dtype=torch.float32, device=x.device)
-    with torch.cuda.device(x.device):
+    with _on_device(x):
         st = _lib().rmsnorm_bwd_noalloc(_ptr(g), ldg, _ptr(x), ldx, _ptr(w), kind,
                                         float(weight_bias), _ptr(rstd), _ptr(g_residual), ldgr, T,
                                         H, _ptr(dx), lddx, _ptr(dw), _stream(x))
