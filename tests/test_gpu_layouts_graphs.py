@@ -129,3 +129,39 @@ def test_cuda_graph_replay_matches_eager():
         want = [y, hn, dx, dw, rstd]
         for a, b, name in zip(got, want, ("y", "h_new", "dx", "dw", "rstd")):
             assert torch.equal(a, b), (seed, name)
+
+
+def test_back_to_back_dependent_calls_match_serialised_calls():
+    # Every grid is launched with programmatic dependent launch, so the next
+    # grid may be scheduled while the previous one still runs; each call here
+    # reads what the call before it wrote (forward -> backward -> forward on
+    # the backward's dx ...), so a missing dependency wait would read stale
+    # rows.  The chain enqueued back to back equals the same chain with a
+    # device synchronisation after every call, bit for bit.
+    T, H = 3000, 2048
+    xb, gb = synth.random_rows(50, T, H, n=2)
+    w = gu.dev_bf16(synth.random_weight(50, H))
+    ws = crm.rmsnorm_bwd_workspace(T, H, gu.DEV)
+
+    def chain(sync):
+        x = gu.dev_bf16(xb)
+        g = gu.dev_bf16(gb)
+        outs = []
+        for _ in range(6):
+            y, rstd, _ = crm.rmsnorm_fwd(x, w, 1e-6)
+            if sync:
+                torch.cuda.synchronize()
+            dx, dw = crm.rmsnorm_bwd(g, y, w, rstd, workspace=ws)
+            if sync:
+                torch.cuda.synchronize()
+            q = torch.empty((T, H), dtype=torch.float8_e4m3fn, device=gu.DEV)
+            crm.rmsnorm_quant(q, dx, w, 0.5)
+            if sync:
+                torch.cuda.synchronize()
+            outs += [y, rstd, dx, dw, q.view(torch.uint8)]
+            x, g = dx, y
+        torch.cuda.synchronize()
+        return outs
+
+    for a, b in zip(chain(False), chain(True)):
+        assert torch.equal(a, b)
