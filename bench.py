@@ -252,6 +252,13 @@ def other_kernels(dev, peak):
         return lambda: crm.fused_add_rmsnorm_quant(q, x, r, w, sc)
     add("fused_add_rmsnorm_quant e4m3 T=H=8192", quant, 469_778_436)
 
+    def plain_quant():
+        x, w = randn(8192, 8192), randn(8192, scale=0.1, shift=1.0)
+        q = torch.empty((8192, 8192), dtype=torch.float8_e4m3fn, device=dev)
+        return lambda: crm.rmsnorm_quant(q, x, w, sc)
+    # read x (2 B), write q (1 B) per element; w once
+    add("rmsnorm_quant e4m3 (no residual) T=H=8192", plain_quant, 8192 * 8192 * 3 + 8192 * 2)
+
     def block():
         x, r, w = randn(8192, 8192), randn(8192, 8192), randn(8192, scale=0.1, shift=1.0)
         q = torch.empty((8192, 8192), dtype=torch.float8_e4m3fn, device=dev)

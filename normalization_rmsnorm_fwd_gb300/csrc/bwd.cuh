@@ -23,9 +23,12 @@
 // pipeline (row i+1's sum formed while row i gets its dx, one CTA barrier per
 // row); the per-row integer work is kept to running pointers and counters,
 // since at about 20 instructions per element the kernel is bound by issue.
-// At the end the CTA adds its row groups in group order and writes one FP32
-// partial row; a second kernel (bwd_reduce.cu) adds the partial rows of each
-// column in a fixed order.
+// D is 3, 2 or 1 rows: the deepest ring that fits the shared-memory budget.
+// At the end the CTA adds its row groups in group order, column-parallel
+// across its threads, and writes one FP32 partial row; a second kernel
+// (bwd_reduce.cu) adds the partial rows of each column in a fixed order.
+// Both grids are launched with programmatic dependent launch and wait for
+// the preceding grid before touching global memory.
 #pragma once
 
 #include <atomic>

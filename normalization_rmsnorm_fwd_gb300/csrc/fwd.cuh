@@ -25,11 +25,14 @@
 // eps), o = (h - mean)*rstd*gamma + beta.
 //
 // Two launch forms.  One row per group per CTA (LOOP = false): a grid of
-// ceil(T / rpc) CTAs.  Persistent (LOOP = true, the plain row with the y or
-// static FP8 epilogue, which streams a single input): a grid of resident CTAs
-// whose groups walk the rows with a stride of the whole grid; the weights are
-// loaded once per CTA and the next row's x is loaded before the current row
-// is reduced and written, so its loads are in flight during that work.
+// ceil(T / rpc) CTAs.  Persistent (LOOP = true: the plain row with the y or
+// static FP8 epilogue, and LayerNorm with gamma and beta in shared memory;
+// each streams a single input): a grid of resident CTAs whose groups walk the
+// rows with a stride of the whole grid; the weights are loaded once per CTA
+// and the next row's x is fetched ahead (into registers, or into L2 only) so
+// its loads are in flight while the current row is reduced and written.
+// Every grid is launched with programmatic dependent launch and waits for
+// the preceding grid before touching global memory.
 #pragma once
 
 #include <atomic>
@@ -132,12 +135,11 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
                 ld_f32_keep<VEC>(static_cast<const float *>(p.w) + c, wf[k]);
             else
                 wb[k] = ld_keep<VEC>(static_cast<const uint16_t *>(p.w) + c);
-            if constexpr (LN) ld_f32_keep<VEC>(p.beta + c, bt[k]);
         } else {
 #pragma unroll
             for (int i = 0; i < NW; ++i) wb[k].w[i] = 0u;
 #pragma unroll
-            for (int i = 0; i < VEC; ++i) { wf[k][i] = 0.f; bt[k][i] = 0.f; }
+            for (int i = 0; i < VEC; ++i) wf[k][i] = 0.f;
         }
     };
     auto load_weights = [&]() {
