@@ -425,6 +425,16 @@ def run_ours(args):
     fwd_us = sum(e[0].elapsed_time(e[1]) for e in evs) / nsplit * 1e3
     bwd_us = sum(e[1].elapsed_time(e[2]) for e in evs) / nsplit * 1e3
 
+    def spread(vals):
+        q = statistics.quantiles(vals, n=10)
+        return {"median": round(statistics.median(vals), 2), "p10": round(q[0], 2),
+                "p90": round(q[8], 2), "n": len(vals)}
+    distribution_us = {
+        "forward": spread([e[0].elapsed_time(e[1]) * 1e3 for e in evs]),
+        "backward": spread([e[1].elapsed_time(e[2]) * 1e3 for e in evs]),
+        "step": spread([e[0].elapsed_time(e[2]) * 1e3 for e in evs]),
+    }
+
     # End to end through the public API with host buffers: every step copies
     # its inputs in from pinned host memory, runs both calls and copies every
     # output back, all inside the timing.  Steps are pipelined over two
@@ -532,6 +542,7 @@ def run_ours(args):
                      "bytes_per_call": BWD_BYTES, "us_per_call": round(bwd_us, 2),
                      "launches_per_call": 2, "traffic": ncu_traffic("rmsnorm_bwd")},
         "clocks": clock,
+        "per_step_us": distribution_us,
         "e2e": e2e,
         "gpu_launches": 3 * args.steps,
         "per_kernel": per_kernel,
