@@ -554,16 +554,11 @@ cudaError_t launch_bwd_inst(BwdParams p, int sms, int *nchunk_out, cudaStream_t 
     const int threads = p.tpr * p.rpc;
     const size_t smem = bwd_smem_bytes(GRES, VEC, VPT, threads, p.rpc, p.H, D);
     auto kern = k_rmsnorm_bwd<W32, GRES, VEC, VPT, SUB, D>;
-    // Opt in to more than the default dynamic shared memory once per kernel
-    // (the largest size requested so far is remembered).
-    static std::atomic<int> opted{0};
-    if ((int)smem > opted.load(std::memory_order_relaxed)) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        opted.store((int)smem, std::memory_order_relaxed);
-    }
+    static std::atomic<int> opted[kOptInDevices];
+    cudaError_t e = opt_in_smem(kern, smem, opted);
+    if (e != cudaSuccess) return e;
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaErrorInvalidConfiguration;
     if (per_sm > kBwdMaxCtasPerSm) per_sm = kBwdMaxCtasPerSm;

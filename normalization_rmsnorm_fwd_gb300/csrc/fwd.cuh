@@ -536,15 +536,9 @@ cudaError_t launch_fwd_kernel(const FwdParams &p, size_t smem, cudaStream_t s)
     const int threads = p.tpr * p.rpc;
     int64_t blocks = (p.T + p.rpc - 1) / p.rpc;
     if (smem > 0) {
-        // Opt in to dynamic shared memory beyond the default (which, with the
-        // kernel's static shared memory, must stay within 48 KB); the largest
-        // size requested so far is remembered.
-        static std::atomic<long long> opted{0};
-        if ((long long)smem > opted.load(std::memory_order_relaxed)) {
-            cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return e;
-            opted.store((long long)smem, std::memory_order_relaxed);
-        }
+        static std::atomic<int> opted[kOptInDevices];
+        cudaError_t e = opt_in_smem(kern, smem, opted);
+        if (e != cudaSuccess) return e;
     }
     if constexpr (LOOP) {
         // threads << 40 | shared-memory bytes << 8 | CTAs per SM

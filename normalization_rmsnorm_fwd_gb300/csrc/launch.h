@@ -2,6 +2,7 @@
 // host ABI (api.cu) and the kernel translation units.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -71,6 +72,32 @@ struct Layout {
 };
 
 // Forward launches, one per epilogue family (fwd_*.cu).
+// Devices whose dynamic shared-memory opt-in is remembered (beyond them the
+// attribute is simply set on every launch that needs it).
+constexpr int kOptInDevices = 64;
+
+// Lets kern use `smem` bytes of dynamic shared memory on the current device
+// (cudaFuncSetAttribute acts on the current device's context, and the
+// default allows 48 KB including the kernel's static shared memory).
+// `opted` is the caller's per-kernel record of the largest size set on each
+// device, so the attribute is set once per kernel, device and larger size.
+template <typename Kernel>
+cudaError_t opt_in_smem(Kernel kern, size_t smem, std::atomic<int> (&opted)[kOptInDevices])
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool tracked = dev >= 0 && dev < kOptInDevices;
+    if (tracked && (int)smem <= opted[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess && tracked) {
+        int cur = opted[dev].load(std::memory_order_relaxed);
+        while ((int)smem > cur && !opted[dev].compare_exchange_weak(cur, (int)smem)) {
+        }
+    }
+    return e;
+}
+
 // Launches kern<<<grid, block, smem, s>>>(args...) with programmatic
 // dependent launch allowed: the grid may be scheduled while the kernel before
 // it in the stream is still running.  Every kernel of this library that is
