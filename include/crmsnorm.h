@@ -175,7 +175,11 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t rows, int64_t H, int device,
  * The scratch is a 16 MiB array in the library's own device memory, held by
  * every GPU that loads the library until the process exits.  The first call
  * on a device looks up the array's device address (cudaGetSymbolAddress with
- * that device current); make that first call before any stream capture.  All
+ * that device current); make that first call before any stream capture.  The
+ * address is kept per device number for the life of the process, so it is
+ * only valid in the context that made the first call: calls after
+ * cudaDeviceReset on that device, or from a context other than the device's
+ * primary context (the one the runtime API uses), are not supported.  All
  * calls on a device share the array: calls that overlap on the GPU (other
  * streams or host threads) race and must be serialised.  The scratch needs
  * no zeroing.  Problems whose workspace (rmsnorm_bwd_workspace_bytes) exceeds

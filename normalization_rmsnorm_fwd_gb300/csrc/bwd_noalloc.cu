@@ -13,7 +13,9 @@
 // uses the array's name as a pointer (on the host it is only a stand-in):
 // the first call on each device looks up its device address with
 // cudaGetSymbolAddress while that device is current, and later calls reuse
-// the cached address.  All calls on a device share the one array, so calls
+// the cached address (valid in the device's primary context only: a
+// cudaDeviceReset or a non-primary context would need a new lookup, which
+// the header documents as unsupported).  All calls on a device share the one array, so calls
 // that run at the same time on the GPU (different streams, or different host
 // threads) overwrite each other's scratch and race; serialise them on one
 // stream.  The scratch needs no initial value: the backward writes every

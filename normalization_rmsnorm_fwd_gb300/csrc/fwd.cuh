@@ -99,7 +99,13 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
     constexpr int NW = VEC / 2;
     constexpr bool ADA = (OUT == OUT_ADA || OUT == OUT_ADA_Q);
     constexpr bool LN = (IN == IN_LAYERNORM);
-    __shared__ float red_h[32], red_l[32];
+    // Per-warp partial sums of a multi-warp row group.  The persistent form
+    // alternates two planes by row parity: the warps of a group write row
+    // i+1's slots while slower warps may still read row i's, and only the
+    // barrier of row i+1 orders those writes after row i's reads, so row
+    // i+2 can reuse plane i's slots.  LayerNorm's two reductions per row
+    // already alternate red2_h and red_h, a barrier between every reuse.
+    __shared__ float red_h[2][32], red_l[2][32];
     __shared__ float red2_h[LN ? 32 : 1];
     // Programmatic dependent launch: wait for the preceding grid (and its
     // memory) before any global access; let the next grid be scheduled now
@@ -197,7 +203,7 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
         scale_v = p.scale != nullptr ? __ldg(p.scale) : 1.f;
     const DivScale dsc(scale_v);            // IEEE division by the scale
 
-    auto process = [&](int64_t t) {
+    auto process = [&](int64_t t, int par) {
         const bool live = t < p.T;
         // ---------------- phase 2: normalised input h, sum of squares ---------
         BVec<VEC> h[VPT];
@@ -311,8 +317,8 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
                 p.mean[t] = mean;
         }
         float ssum;
-        if constexpr (LN) ssum = row_sum_plain(ss2, red_h);
-        else ssum = row_sum(ss2, red_h, red_l);
+        if constexpr (LN) ssum = row_sum_plain(ss2, red_h[0]);
+        else ssum = row_sum(ss2, red_h[par], red_l[par]);
         reunpack();
         const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ssum, (float)p.H), p.eps)));
         if (p.rstd != nullptr && live && lane == 0)
@@ -457,7 +463,7 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
     if constexpr (!LOOP) {
         const int64_t t = (int64_t)blockIdx.x * p.rpc + grp;
         load_row(t, xa, true);
-        process(t);
+        process(t, 0);
     } else {
         static_assert(IN == IN_PLAIN || LN, "the persistent form streams one input");
         load_weights();
@@ -489,7 +495,8 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
         // The next row is loaded into registers before this row is processed
         // (PF == 2), or only prefetched into L2 then and loaded afterwards
         // (PF == 1: no registers held across the row).
-        for (int64_t base = b0; base < p.T; base += stride) {
+        int par = 0;
+        for (int64_t base = b0; base < p.T; base += stride, par ^= 1) {
             BVec<VEC> xn[VPT];
             const bool more = base + stride < p.T;   // the same for the whole CTA
             const int64_t tn = base + stride + grp;
@@ -505,7 +512,7 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
                     }
                 }
             }
-            process(base + grp);
+            process(base + grp, par);
             if (more) {
                 if constexpr (PF == 2) {
 #pragma unroll

@@ -4,6 +4,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <mutex>
 #include <cuda_runtime.h>
 
 #include "common.cuh"
@@ -81,6 +82,15 @@ constexpr int kOptInDevices = 64;
 // default allows 48 KB including the kernel's static shared memory).
 // `opted` is the caller's per-kernel record of the largest size set on each
 // device, so the attribute is set once per kernel, device and larger size.
+// A miss sets the attribute to the larger of the request and the recorded
+// size, under one lock with the record update, so two threads asking for
+// different sizes can never leave the attribute below the record.
+inline std::mutex &opt_in_mutex()
+{
+    static std::mutex m;
+    return m;
+}
+
 template <typename Kernel>
 cudaError_t opt_in_smem(Kernel kern, size_t smem, std::atomic<int> (&opted)[kOptInDevices])
 {
@@ -88,13 +98,14 @@ cudaError_t opt_in_smem(Kernel kern, size_t smem, std::atomic<int> (&opted)[kOpt
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const bool tracked = dev >= 0 && dev < kOptInDevices;
-    if (tracked && (int)smem <= opted[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+    if (!tracked)
+        return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if ((int)smem <= opted[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(opt_in_mutex());
+    const int cur = opted[dev].load(std::memory_order_relaxed);
+    if ((int)smem <= cur) return cudaSuccess;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e == cudaSuccess && tracked) {
-        int cur = opted[dev].load(std::memory_order_relaxed);
-        while ((int)smem > cur && !opted[dev].compare_exchange_weak(cur, (int)smem)) {
-        }
-    }
+    if (e == cudaSuccess) opted[dev].store((int)smem, std::memory_order_release);
     return e;
 }
 
