@@ -120,6 +120,18 @@ def random_rows(seed: int, T: int, H: int, scale: float = 1.0, n: int = 1) -> li
     return [d.bf16((T, H), scale) for _ in range(n)]
 
 
+def bf16_codes(seed: int, shape, lo: int, hi: int, signed: bool = True) -> np.ndarray:
+    """BF16 bit patterns whose magnitude codes are drawn uniformly from
+    [lo, hi) (0x0001..0x007F are the subnormals, 0x0080 is 2^-126) with, when
+    `signed`, a random sign bit (edge-case tests near the bottom of the
+    range)."""
+    g = torch.Generator().manual_seed(int(seed))
+    mag = torch.randint(int(lo), int(hi), tuple(shape), generator=g, dtype=torch.int32)
+    if signed:
+        mag |= torch.randint(0, 2, tuple(shape), generator=g, dtype=torch.int32) << 15
+    return mag.numpy().astype(np.uint16)
+
+
 def random_weight(seed: int, H: int, f32: bool = False) -> np.ndarray:
     """BF16 w = 1 + 0.1 N(0,1), or FP32 zero-centred w = 0.02 N(0,1)."""
     d = Draw(seed)

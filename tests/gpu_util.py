@@ -18,6 +18,9 @@ Tolerances (the pages' accuracy contract as restated for this library):
 """
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 import torch
 
@@ -102,10 +105,23 @@ def dx_allowance(g_bits, x_bits, w_eff, rstd, m):
     return 2.0 ** -20 * (np.abs(r * g * w_eff[None, :]) + np.abs(x * r ** 3 * np.asarray(m)[:, None]))
 
 
-def sample_rows(T: int, n: int = 384, seed: int = 0) -> np.ndarray:
-    """First and last rows plus an even spread, sorted, unique."""
-    if T <= n:
-        return np.arange(T)
-    rng = np.random.default_rng(seed)
-    s = np.concatenate([np.arange(8), np.arange(T - 8, T), rng.choice(T, n - 16, replace=False)])
-    return np.unique(s)
+def row_blocks(T: int, H: int, budget: int = 1 << 20) -> list:
+    """Consecutive row ranges [lo, hi) of about `budget` elements each."""
+    rows = max(1, budget // max(int(H), 1))
+    return [(lo, min(T, lo + rows)) for lo in range(0, T, rows)]
+
+
+def each_block(T: int, H: int, fn, budget: int = 1 << 20):
+    """Call fn(lo, hi) for every row block of a [T, H] problem on the host's
+    cores and return the results in block order.  The oracle's C calls and
+    numpy's whole-array operations release the interpreter lock, so the
+    blocks run in parallel; the oracle itself stays single-threaded, each
+    call seeing only its own rows.  The first failing block's error is
+    raised."""
+    blocks = row_blocks(T, H, budget)
+    n = min(len(blocks), os.cpu_count() or 1, 16)
+    if n <= 1:
+        return [fn(lo, hi) for lo, hi in blocks]
+    with ThreadPoolExecutor(max_workers=n) as ex:
+        futs = [ex.submit(fn, lo, hi) for lo, hi in blocks]
+        return [f.result() for f in futs]

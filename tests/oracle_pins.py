@@ -38,8 +38,8 @@ def _bits(vals) -> np.ndarray:
 
 
 def _eval(expr: str, eps32: float = 0.0) -> float:
-    env = {"sqrt": math.sqrt, "eps32": eps32, "nan": math.nan, "inf": math.inf,
-           "f32": lambda v: float(np.float32(v))}
+    env = {"sqrt": math.sqrt, "log": math.log, "e": math.e, "eps32": eps32, "nan": math.nan,
+           "inf": math.inf, "f32": lambda v: float(np.float32(v))}
     return float(eval(expr.replace("^", "**"), {"__builtins__": {}}, env))
 
 
@@ -407,6 +407,11 @@ def pin_block_quant(o):
             v32 = (blk / np.float64(s)).astype(np.float32).astype(np.float64)
             assert np.array_equal(codes, numfmt.nearest_fp8(v32, 0)), (t, b)
     assert np.isnan(r["block_scale"][:, T:]).all()
+
+
+def pin_golden_block_quant(o):
+    """Hand-derived block: a constant row normalises to 1, the block scale is
+    f32(1/448) and every code is 448 (0x7E)."""
     g = json.load(open(GOLDEN))["block_quant"][0]
     Hc = g["H"]
     one = o.fused_add_rmsnorm_fp8_block_quant(
@@ -415,6 +420,91 @@ def pin_block_quant(o):
     assert np.all(numfmt.decode_bf16(one["normed"]) == _eval(g["normed"]))
     assert np.all(one["block_scale"][:, :2] == np.float32(_eval(g["scale"])))
     assert np.all(one["q"] == int(g["code"], 16))
+
+
+def _codes(hexes):
+    return [None if h is None else int(h, 16) for h in hexes]
+
+
+def pin_golden_static_fp8(o):
+    """Hand-derived static-scale FP8 cases: v = y / scale and the codes placed
+    on the E4M3 / E5M2 grids by hand (divide, not multiply; saturation;
+    the residual route)."""
+    g = json.load(open(GOLDEN))
+    for c in g["static_fp8"]:
+        x, w = _bits([c["x"]]), _bits(c["w"])
+        res = _bits([c["residual"]]) if "residual" in c else None
+        for kind, key in ((0, "e4m3"), (1, "e5m2")):
+            if key not in c:
+                continue
+            r = o.rmsnorm_quant(x, w, c["scale"], c["eps"], residual=res, weight_bias=c["bias"],
+                                fp8_kind=kind)
+            _close(r["v_exact"][0], [_eval(e) for e in c["v"]], 4e-16, c["name"] + " v")
+            assert list(r["q"][0]) == _codes(c[key]), (c["name"], key, list(r["q"][0]))
+            if res is not None:
+                _close(numfmt.decode_bf16(r["h_new"][0]), [_eval(e) for e in c["h_new"]], 0,
+                       c["name"] + " h_new")
+
+
+def pin_golden_ada(o):
+    """Hand-derived AdaRMSNorm row: out = norm * (1 + scale) + shift exactly,
+    gate_out the style's last third."""
+    g = json.load(open(GOLDEN))
+    for c in g["ada"]:
+        style = _bits([c["sc"] + c["sh"] + c["gate"]])
+        r = o.ada_rms_norm_style(_bits([c["x"]]), _bits(c["w"]), style, c["eps"])
+        want = [_eval(e) for e in c["out"]]
+        _close(r["out_exact"][0], want, 0, c["name"] + " out")
+        _close(numfmt.decode_bf16(r["out"][0]), want, 0, c["name"] + " out (BF16)")
+        assert np.array_equal(r["gate_out"][0], _bits(c["gate"])), c["name"]
+
+
+def pin_golden_gated_ada(o):
+    """Hand-derived gated residual + Ada + E4M3 row: the residual update,
+    v = Ada output / scale, and the codes placed by hand."""
+    g = json.load(open(GOLDEN))
+    for c in g["gated_ada"]:
+        style = _bits([c["sc"] + c["sh"] + c["gate_chunk"]])
+        r = o.gate_residual_ada_norm_fp8(_bits([c["residual"]]), _bits([c["x"]]), _bits([c["gate"]]),
+                                         _bits(c["w"]), style, c["scale"], c["eps"])
+        _close(numfmt.decode_bf16(r["residual_out"][0]), [_eval(e) for e in c["residual_out"]], 0,
+               c["name"] + " residual")
+        _close(r["v_exact"][0], [_eval(e) for e in c["v"]], 4e-16, c["name"] + " v")
+        assert list(r["q"][0]) == _codes(c["e4m3"]), (c["name"], list(r["q"][0]))
+        assert np.array_equal(r["gate_out"][0], _bits(c["gate_chunk"])), c["name"]
+
+
+def pin_golden_silu(o):
+    """Hand-derived SiLU values: SiLU(0) = 0, SiLU(+-ln 3) = (3/4) ln 3 and
+    -(1/4) ln 3, SiLU(1) = e/(1+e), and E4M3 codes at scale 1/2."""
+    g = json.load(open(GOLDEN))
+    for c in g["silu"]:
+        w32 = np.array([_eval(e) for e in c["w32"]], np.float32)
+        x = _bits([c["x"]])
+        r = o.fused_rmsnorm_silu(x, w32, c["eps"])
+        _close(r["v_exact"][0], [_eval(e) for e in c["v"]], c["rel"], c["name"] + " v")
+        q = o.fused_rmsnorm_silu(x, w32, c["eps"], fp8=True, scale=c["scale"])
+        for got, want in zip(q["q"][0], _codes(c["e4m3"])):
+            assert want is None or got == want, (c["name"], list(q["q"][0]))
+
+
+def pin_golden_layernorm(o):
+    """Hand-derived two-element LayerNorm row: mean, rstd (population
+    variance, eps inside the root), the output with gamma and beta, and its
+    FP8 codes (an E5M2 tie rounded to even)."""
+    g = json.load(open(GOLDEN))
+    for c in g["layernorm"]:
+        x = _bits([c["x"]])
+        gamma, beta = np.array(c["gamma"], np.float32), np.array(c["beta"], np.float32)
+        r = o.layernorm(x, gamma, beta, c["eps"])
+        _close(r["mean"][0], _eval(c["mean"]), 0, c["name"] + " mean")
+        _close(r["rstd"][0], _eval(c["rstd"]), 1e-15, c["name"] + " rstd")
+        want = [_eval(e) for e in c["y"]]
+        _close(r["v_exact"][0], want, 1e-15, c["name"] + " y")
+        _close(numfmt.decode_bf16(r["y"][0]), want, 0, c["name"] + " y (BF16)")
+        for kind, key in ((0, "e4m3"), (1, "e5m2")):
+            q = o.layernorm(x, gamma, beta, c["eps"], fp8_kind=kind, scale=c["scale"])
+            assert list(q["q"][0]) == _codes(c[key]), (c["name"], key, list(q["q"][0]))
 
 
 # ------------------------------------------------------------------- Ada --

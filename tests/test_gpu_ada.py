@@ -37,17 +37,13 @@ def compare_ada(orc, x, w, style, eps=1e-6):
     gu.check_exact(gu.host_bits(gate_out), ref["gate_out"], "gate_out")
 
 
-def compare_gated(orc, u, x, gate, w, style, scale=0.04, eps=1e-6, rows=None):
+def compare_gated(orc, u, x, gate, w, style, scale=0.04, eps=1e-6):
     ud = gu.dev_bf16(u)
     res, out, gate_out = crm.gate_residual_ada_norm_fp8(ud, gu.dev_bf16(x), gu.dev_bf16(gate),
                                                         gu.dev_bf16(w), gu.dev_bf16(style),
                                                         scale, eps)
     torch.cuda.synchronize()
     r_gpu, q_gpu, g_gpu = gu.host_bits(res), gu.host_u8(out), gu.host_bits(gate_out)
-    if rows is not None:
-        u, x, gate, r_gpu, q_gpu, g_gpu = u[rows], x[rows], gate[rows], r_gpu[rows], q_gpu[rows], g_gpu[rows]
-        if style.shape[0] > 1:
-            style = style[rows]
     ref = orc.gate_residual_ada_norm_fp8(u, x, gate, w, style, scale, eps)
     gu.check_exact(r_gpu, ref["residual_out"], "residual")
     gu.check_exact(g_gpu, ref["gate_out"], "gate_out")

@@ -27,20 +27,34 @@ def run_bwd(g, x, w, rstd, bias=0.0, g_res=None, workspace=None):
     return gu.host_bits(dx), dw.cpu().numpy()
 
 
-def compare(orc, g, x, w, eps=1e-6, bias=0.0, g_res=None, rows=None):
-    rstd = orc.rmsnorm_fwd(x, w, eps, weight_bias=bias, want_y=False)["rstd"]
-    dx, dw = run_bwd(g, x, w, rstd, bias, g_res)
-    full = orc.rmsnorm_bwd(g, x, w, rstd, weight_bias=bias, g_res=g_res, want_dx=rows is None)
-    gu.check_dw(dw, full["dw"], full["dw_abs"])
-    if rows is None:
-        ref, sel = full, slice(None)
-    else:
-        sel = rows
-        ref = orc.rmsnorm_bwd(g[rows], x[rows], w, rstd[rows], weight_bias=bias,
-                              g_res=None if g_res is None else g_res[rows])
+def oracle_rstd(orc, x, w, eps, bias=0.0):
+    """The oracle forward's FP32 rstd of every row (row blocks in parallel)."""
+    T, H = x.shape
+    parts = gu.each_block(T, H, lambda lo, hi: orc.rmsnorm_fwd(x[lo:hi], w, eps, weight_bias=bias,
+                                                               want_y=False)["rstd"])
+    return np.concatenate(parts) if parts else np.empty(0, np.float32)
+
+
+def check_every_row(orc, g, x, w, rstd, dx, dw, bias=0.0, g_res=None):
+    """dx of every row against the oracle, and dw against the oracle's sum
+    over all rows (formed block by block in double precision)."""
+    T, H = x.shape
     w_eff = orc.weight_eff(w, bias)
-    allow = gu.dx_allowance(g[sel], x[sel], w_eff, rstd[sel], ref["m"])
-    gu.check_bf16(dx[sel], ref["dx_exact"], allowance=allow, what="dx")
+
+    def check(lo, hi):
+        gr = None if g_res is None else g_res[lo:hi]
+        ref = orc.rmsnorm_bwd(g[lo:hi], x[lo:hi], w, rstd[lo:hi], weight_bias=bias, g_res=gr)
+        allow = gu.dx_allowance(g[lo:hi], x[lo:hi], w_eff, rstd[lo:hi], ref["m"])
+        gu.check_bf16(dx[lo:hi], ref["dx_exact"], allowance=allow, what=f"dx rows {lo}:{hi}")
+        return ref["dw"], ref["dw_abs"]
+    parts = gu.each_block(T, H, check)
+    gu.check_dw(dw, sum(p[0] for p in parts), sum(p[1] for p in parts))
+
+
+def compare(orc, g, x, w, eps=1e-6, bias=0.0, g_res=None):
+    rstd = oracle_rstd(orc, x, w, eps, bias)
+    dx, dw = run_bwd(g, x, w, rstd, bias, g_res)
+    check_every_row(orc, g, x, w, rstd, dx, dw, bias, g_res)
     return dx, dw
 
 
@@ -66,21 +80,24 @@ def test_widths_and_routes(orc, H, route):
 def test_row_counts(orc, T):
     g, x = synth.random_rows(T, T, 512, n=2)
     w = synth.random_weight(T, 512)
-    compare(orc, g, x, w, rows=None if T < 1000 else gu.sample_rows(T))
+    compare(orc, g, x, w)
 
 
 def test_residual_large_config(orc):
     """T=16384, H=4096 on the residual route: the backward of h_new with the
-    gradient g; dw over all rows, dx on a spread of rows."""
+    gradient g; dx on every row, dw over all rows."""
     d = synth.residual_large()
-    h_new = orc.rmsnorm_fwd(d["x"], d["w"], d["eps"], residual=d["residual"], want_y=False)["h_new"]
-    compare(orc, d["g"], h_new, d["w"], d["eps"], rows=gu.sample_rows(d["T"]))
+    T, H = d["T"], d["H"]
+    h_new = np.concatenate(gu.each_block(T, H, lambda lo, hi: orc.rmsnorm_fwd(
+        d["x"][lo:hi], d["w"], d["eps"], residual=d["residual"][lo:hi], want_y=False)["h_new"]))
+    compare(orc, d["g"], h_new, d["w"], d["eps"])
 
 
-@pytest.mark.parametrize("T", [1024, 4096])
+@pytest.mark.parametrize("T", [1, 7, 128, 1024, 1025, 4096, 16384])
 def test_zero_centred_weight_config(orc, T):
+    """H=5120, FP32 zero-centred weight, every row of every token count."""
     d = synth.zero_centred(T)
-    compare(orc, d["g"], d["x"], d["w"], d["eps"], bias=1.0, rows=gu.sample_rows(T, 256))
+    compare(orc, d["g"], d["x"], d["w"], d["eps"], bias=1.0)
 
 
 def test_strided_heads_config(orc):
@@ -98,8 +115,8 @@ def test_strided_heads_config(orc):
     torch.cuda.synchronize()
     gu.check_exact(gu.host_bits(dx), gu.host_bits(dxc), "strided vs contiguous dx")
     assert torch.equal(dw, dwc)
-    ref = orc.rmsnorm_bwd(g2, x2, d["w"], rstd, weight_bias=1.0, want_dx=False)
-    gu.check_dw(dw.cpu().numpy(), ref["dw"], ref["dw_abs"])
+    check_every_row(orc, g2, x2, d["w"], rstd, gu.host_bits(dx).reshape(-1, H),
+                    dw.cpu().numpy(), bias=1.0)
 
 
 def test_dw_is_bitwise_reproducible():
@@ -169,5 +186,5 @@ def test_pipelined_chunk_lengths(orc, H, T):
     # H = 1024).
     g, x = synth.random_rows(T + H, T, H, n=2)
     w = synth.random_weight(T + 7, H)
-    compare(orc, g, x, w, rows=None if T < 1000 else gu.sample_rows(T))
+    compare(orc, g, x, w)
 

@@ -27,18 +27,20 @@ def run_fwd(x_bits, w, eps=1e-6, residual_bits=None, bias=0.0):
             gu.host_bits(h_new) if h_new is not None else None)
 
 
-def compare(orc, x, w, eps=1e-6, residual=None, bias=0.0, rows=None):
+def compare(orc, x, w, eps=1e-6, residual=None, bias=0.0):
+    """Every row of the GPU forward against the oracle (row blocks checked on
+    the host's cores)."""
     y, rstd, h_new = run_fwd(x, w, eps, residual, bias)
-    if rows is not None:
-        x = x[rows]
-        residual = residual[rows] if residual is not None else None
-        y, rstd = y[rows], rstd[rows]
-        h_new = h_new[rows] if h_new is not None else None
-    ref = orc.rmsnorm_fwd(x, w, eps, residual=residual, weight_bias=bias)
-    gu.check_rstd(rstd, ref["rstd_exact"])
-    gu.check_bf16(y, ref["y_exact"])
-    if residual is not None:
-        gu.check_exact(h_new, ref["h_new"], "h_new")
+    T, H = x.shape
+
+    def check(lo, hi):
+        r = None if residual is None else residual[lo:hi]
+        ref = orc.rmsnorm_fwd(x[lo:hi], w, eps, residual=r, weight_bias=bias)
+        gu.check_rstd(rstd[lo:hi], ref["rstd_exact"], what=f"rstd rows {lo}:{hi}")
+        gu.check_bf16(y[lo:hi], ref["y_exact"], what=f"y rows {lo}:{hi}")
+        if residual is not None:
+            gu.check_exact(h_new[lo:hi], ref["h_new"], f"h_new rows {lo}:{hi}")
+    gu.each_block(T, H, check)
     return y, rstd, h_new
 
 
@@ -66,25 +68,24 @@ def test_row_counts_residual_h4096(orc, T):
 
 
 def test_residual_large_config(orc):
-    """T=16384, H=4096 fused residual route: h_new compared on every row,
-    y and rstd on a spread of rows."""
+    """T=16384, H=4096 fused residual route, every row: h_new bit-exact
+    (against the oracle and against a brute-force nearest-BF16 table of the
+    exact sum), y and rstd within tolerance."""
     d = synth.residual_large()
-    y, rstd, h_new = run_fwd(d["x"], d["w"], d["eps"], d["residual"])
-    hn_ref = numfmt.nearest_bf16(numfmt.decode_bf16(d["x"]) + numfmt.decode_bf16(d["residual"]))
-    gu.check_exact(h_new, hn_ref, "h_new (all rows)")
-    rows = gu.sample_rows(d["T"])
-    ref = orc.rmsnorm_fwd(d["x"][rows], d["w"], d["eps"], residual=d["residual"][rows])
-    gu.check_exact(h_new[rows], ref["h_new"], "h_new vs oracle")
-    gu.check_rstd(rstd[rows], ref["rstd_exact"])
-    gu.check_bf16(y[rows], ref["y_exact"])
+    y, rstd, h_new = compare(orc, d["x"], d["w"], d["eps"], d["residual"])
+
+    def nearest(lo, hi):
+        exact = numfmt.decode_bf16(d["x"][lo:hi]) + numfmt.decode_bf16(d["residual"][lo:hi])
+        gu.check_exact(h_new[lo:hi], numfmt.nearest_bf16(exact), f"h_new rows {lo}:{hi} (table)")
+    gu.each_block(d["T"], d["H"], nearest)
 
 
 @pytest.mark.parametrize("T", [1, 7, 128, 1024, 1025, 4096, 16384])
 def test_zero_centred_weight_config(orc, T):
-    """H=5120, FP32 zero-centred weight (effective 1 + w), x ~ 4 N(0,1)."""
+    """H=5120, FP32 zero-centred weight (effective 1 + w), x ~ 4 N(0,1),
+    every row."""
     d = synth.zero_centred(T)
-    rows = None if T <= 1025 else gu.sample_rows(T)
-    compare(orc, d["x"], d["w"], d["eps"], bias=1.0, rows=rows)
+    compare(orc, d["x"], d["w"], d["eps"], bias=1.0)
 
 
 def test_strided_heads_config(orc):
@@ -105,11 +106,15 @@ def test_strided_heads_config(orc):
     gu.check_exact(gu.host_bits(obuf[..., d["H"]:]), gu.host_bits(y), "strided output")
     assert not obuf[..., :d["H"]].any()
     assert torch.equal(rstd, rstdc)
-    x2 = d["buf"].reshape(-1, d["W"])[:, :d["H"]]
-    rows = gu.sample_rows(x2.shape[0], 512)
-    ref = orc.rmsnorm_fwd(np.ascontiguousarray(x2[rows]), d["w"], d["eps"], weight_bias=1.0)
-    gu.check_bf16(gu.host_bits(y).reshape(-1, d["H"])[rows], ref["y_exact"])
-    gu.check_rstd(rstd.cpu().numpy().reshape(-1)[rows], ref["rstd_exact"])
+    x2 = d["buf"].reshape(-1, d["W"])[:, :d["H"]]        # row stride 256, every row checked
+    yb = gu.host_bits(y).reshape(-1, d["H"])
+    rb = rstd.cpu().numpy().reshape(-1)
+
+    def check(lo, hi):
+        ref = orc.rmsnorm_fwd(x2[lo:hi], d["w"], d["eps"], weight_bias=1.0)
+        gu.check_bf16(yb[lo:hi], ref["y_exact"], what=f"y rows {lo}:{hi}")
+        gu.check_rstd(rb[lo:hi], ref["rstd_exact"], what=f"rstd rows {lo}:{hi}")
+    gu.each_block(x2.shape[0], d["H"], check)
 
 
 def test_in_place_fused_add(orc):
@@ -193,3 +198,44 @@ def test_zero_rows_launch_nothing():
     w = torch.ones(4096, dtype=torch.bfloat16, device=gu.DEV)
     y, rstd, _ = crm.rmsnorm_fwd(x, w)
     assert y.shape == (0, 4096) and rstd.shape == (0,)
+
+
+@pytest.mark.parametrize("H", [1024, 4096, 8192, 16384])
+@pytest.mark.parametrize("form", ["y", "e4m3"])
+def test_persistent_forms_every_row(orc, H, form):
+    """The persistent plain forms (BF16 y and static FP8), whose row groups
+    of one to sixteen warps walk many rows per CTA with shared per-warp
+    reduction slots: at T=16384 every row matches the oracle and is bitwise
+    equal to the same row normalised alone (one launch per row, T=1)."""
+    T = 16384
+    x = synth.random_rows(H + 40, T, H)[0]
+    w = synth.random_weight(H + 41, H)
+    xd, wd = gu.dev_bf16(x), gu.dev_bf16(w)
+    rstd, rstd1 = torch.empty(T, device=gu.DEV), torch.empty(T, device=gu.DEV)
+    if form == "y":
+        out, out1 = torch.empty_like(xd), torch.empty_like(xd)
+        crm.rmsnorm_fwd(xd, wd, 1e-6, y=out, rstd=rstd)
+        for t in range(T):
+            crm.rmsnorm_fwd(xd[t:t + 1], wd, 1e-6, y=out1[t:t + 1], rstd=rstd1[t:t + 1])
+    else:
+        sc = torch.tensor([0.04], device=gu.DEV)
+        out = torch.empty((T, H), dtype=torch.float8_e4m3fn, device=gu.DEV)
+        out1 = torch.empty_like(out)
+        crm.rmsnorm_quant(out, xd, wd, sc, 1e-6, rstd=rstd)
+        for t in range(T):
+            crm.rmsnorm_quant(out1[t:t + 1], xd[t:t + 1], wd, sc, 1e-6, rstd=rstd1[t:t + 1])
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.uint8), out1.view(torch.uint8)), "differs from one row per launch"
+    assert torch.equal(rstd.view(torch.int32), rstd1.view(torch.int32)), "rstd differs from one row per launch"
+    o = gu.host_bits(out) if form == "y" else gu.host_u8(out)
+    r = rstd.cpu().numpy()
+
+    def check(lo, hi):
+        ref = orc.rmsnorm_fwd(x[lo:hi], w, 1e-6, want_y=form == "y")
+        gu.check_rstd(r[lo:hi], ref["rstd_exact"], what=f"rstd rows {lo}:{hi}")
+        if form == "y":
+            gu.check_bf16(o[lo:hi], ref["y_exact"], what=f"y rows {lo}:{hi}")
+        else:
+            q = orc.rmsnorm_quant(x[lo:hi], w, 0.04, 1e-6, fp8_kind=0)
+            gu.check_fp8(o[lo:hi], q["q"], q["v_exact"], 0, what=f"e4m3 rows {lo}:{hi}")
+    gu.each_block(T, H, check)

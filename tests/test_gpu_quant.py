@@ -30,18 +30,21 @@ def run_static(x, w, scale, kind, residual=None, bias=0.0):
     return gu.host_u8(out), (gu.host_bits(r) if r is not None else None), rstd.cpu().numpy()
 
 
-def compare_static(orc, x, w, scale, kind, residual=None, bias=0.0, rows=None):
+def compare_static(orc, x, w, scale, kind, residual=None, bias=0.0):
+    """Every row: codes, the in-place residual and rstd against the oracle."""
     q, h_new, rstd = run_static(x, w, scale, kind, residual, bias)
-    if rows is not None:
-        x, q, rstd = x[rows], q[rows], rstd[rows]
+    T, H = x.shape
+
+    def check(lo, hi):
+        r = None if residual is None else residual[lo:hi]
+        ref = orc.rmsnorm_quant(x[lo:hi], w, scale, 1e-6, residual=r, weight_bias=bias,
+                                fp8_kind=kind)
+        gu.check_fp8(q[lo:hi], ref["q"], ref["v_exact"], kind, what=f"fp8 rows {lo}:{hi}")
         if residual is not None:
-            residual, h_new = residual[rows], h_new[rows]
-    ref = orc.rmsnorm_quant(x, w, scale, 1e-6, residual=residual, weight_bias=bias, fp8_kind=kind)
-    gu.check_fp8(q, ref["q"], ref["v_exact"], kind)
-    if residual is not None:
-        gu.check_exact(h_new, ref["h_new"], "residual in place")
-    r = orc.rmsnorm_fwd(x, w, 1e-6, residual=residual, weight_bias=bias, want_y=False)
-    gu.check_rstd(rstd, r["rstd_exact"])
+            gu.check_exact(h_new[lo:hi], ref["h_new"], f"residual in place, rows {lo}:{hi}")
+        f = orc.rmsnorm_fwd(x[lo:hi], w, 1e-6, residual=r, weight_bias=bias, want_y=False)
+        gu.check_rstd(rstd[lo:hi], f["rstd_exact"], what=f"rstd rows {lo}:{hi}")
+    gu.each_block(T, H, check)
 
 
 @pytest.mark.parametrize("kind", [0, 1])
@@ -60,10 +63,10 @@ def test_static_fp32_weight_and_saturation(orc):
 
 
 def test_static_fp8_config(orc):
-    """T = H = 8192, scale 0.04, E4M3FN: fused add, residual updated in place."""
+    """T = H = 8192, scale 0.04, E4M3FN: fused add, residual updated in place;
+    every row."""
     d = synth.fp8()
-    compare_static(orc, d["x"], d["w"], d["scale"], 0, d["residual"],
-                   rows=gu.sample_rows(d["T"], 256))
+    compare_static(orc, d["x"], d["w"], d["scale"], 0, d["residual"])
 
 
 def run_block(x, r, w, ldT=None):
@@ -78,28 +81,30 @@ def run_block(x, r, w, ldT=None):
     return gu.host_u8(out), bs.cpu().numpy(), gu.host_bits(normed), gu.host_bits(rd)
 
 
-def compare_block(orc, x, r, w, rows=None):
+def compare_block(orc, x, r, w):
+    """Every row: residual, normed_out, block scales and codes."""
     q, bs, normed, h_new = run_block(x, r, w)
     T, H = x.shape
-    if rows is None:
-        rows = np.arange(T)
     assert np.isnan(bs[:, T:]).all(), "padding columns of block_scale were written"
-    ref = orc.fused_add_rmsnorm_fp8_block_quant(x[rows], r[rows], w, 1e-6)
-    q, normed, h_new, bs = q[rows], normed[rows], h_new[rows], bs[:, rows]
-    gu.check_exact(h_new, ref["h_new"], "residual in place")
-    gu.check_bf16(normed, ref["normed_exact"], what="normed_out")
     nb = H // 128
-    same_block = (normed == ref["normed"]).reshape(len(rows), nb, 128).all(axis=2)   # [t, b]
-    s_ref = ref["block_scale"][:, :len(rows)].T                                       # [t, b]
-    s_gpu = bs.T
-    assert np.array_equal(s_gpu[same_block], s_ref[same_block]), "block scale"
-    assert np.all(np.abs(s_gpu - s_ref) <= 2.0 ** -7 * s_ref), "block scale (differing normed)"
-    qb = q.reshape(len(rows), nb, 128)
-    rb = ref["q"].reshape(len(rows), nb, 128)
-    assert np.array_equal(qb[same_block], rb[same_block]), "block codes"
-    d = qb[~same_block].astype(np.int32) - rb[~same_block].astype(np.int32)
-    assert np.all(np.abs(d) <= 1), "block codes in blocks whose normed values differ by an ulp"
-    return int((~same_block).sum())
+
+    def check(lo, hi):
+        n = hi - lo
+        ref = orc.fused_add_rmsnorm_fp8_block_quant(x[lo:hi], r[lo:hi], w, 1e-6)
+        gu.check_exact(h_new[lo:hi], ref["h_new"], f"residual in place, rows {lo}:{hi}")
+        gu.check_bf16(normed[lo:hi], ref["normed_exact"], what=f"normed_out rows {lo}:{hi}")
+        same_block = (normed[lo:hi] == ref["normed"]).reshape(n, nb, 128).all(axis=2)   # [t, b]
+        s_ref = ref["block_scale"][:, :n].T                                             # [t, b]
+        s_gpu = bs[:, lo:hi].T
+        assert np.array_equal(s_gpu[same_block], s_ref[same_block]), f"block scale rows {lo}:{hi}"
+        assert np.all(np.abs(s_gpu - s_ref) <= 2.0 ** -7 * s_ref), "block scale (differing normed)"
+        qb = q[lo:hi].reshape(n, nb, 128)
+        rb = ref["q"].reshape(n, nb, 128)
+        assert np.array_equal(qb[same_block], rb[same_block]), f"block codes rows {lo}:{hi}"
+        d = qb[~same_block].astype(np.int32) - rb[~same_block].astype(np.int32)
+        assert np.all(np.abs(d) <= 1), "block codes in blocks whose normed values differ by an ulp"
+        return int((~same_block).sum())
+    return sum(gu.each_block(T, H, check))
 
 
 @pytest.mark.parametrize("H", [128, 256, 384, 1024, 4096, 8192, 16384])
@@ -113,4 +118,4 @@ def test_block_small(orc, H, T):
 
 def test_block_fp8_config(orc):
     d = synth.fp8()
-    compare_block(orc, d["x"], d["residual"], d["w"], rows=gu.sample_rows(d["T"], 256))
+    compare_block(orc, d["x"], d["residual"], d["w"])

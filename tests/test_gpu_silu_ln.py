@@ -32,22 +32,28 @@ def _silu_gpu(x, w, bias=0.0, fp8=False, scale=None, out=None):
     return y, rstd
 
 
-def _check_silu(orc, x, w, bias=0.0, rows=None):
+def _check_silu(orc, x, w, bias=0.0):
+    """Every row: BF16 output, rstd, and E4M3 codes with and without a
+    scale."""
+    T, H = x.shape
     y, rstd = _silu_gpu(x, w, bias)
-    xs = x if rows is None else x[rows]
-    ref = orc.fused_rmsnorm_silu(xs, w, 1e-6, weight_bias=bias)
-    got = gu.host_bits(y)
-    got = got if rows is None else got[rows]
-    gu.check_bf16(got, ref["v_exact"], what="silu bf16")
-    r = rstd.cpu().numpy()
-    gu.check_rstd(r if rows is None else r[rows], ref["rstd"].astype(np.float64))
+    got, r = gu.host_bits(y), rstd.cpu().numpy()
+    qs = {}
     for scale in (None, 0.04):
         q, _ = _silu_gpu(x, w, bias, fp8=True, scale=scale)
-        refq = orc.fused_rmsnorm_silu(xs, w, 1e-6, weight_bias=bias, fp8=True,
-                                      scale=1.0 if scale is None else scale)
-        gq = gu.host_u8(q)
-        gu.check_fp8(gq if rows is None else gq[rows], refq["q"], refq["v_exact"], 0,
-                     what=f"silu e4m3 scale={scale}")
+        qs[scale] = gu.host_u8(q)
+        del q
+
+    def check(lo, hi):
+        ref = orc.fused_rmsnorm_silu(x[lo:hi], w, 1e-6, weight_bias=bias)
+        gu.check_bf16(got[lo:hi], ref["v_exact"], what=f"silu bf16 rows {lo}:{hi}")
+        gu.check_rstd(r[lo:hi], ref["rstd"].astype(np.float64), what=f"rstd rows {lo}:{hi}")
+        for scale, gq in qs.items():
+            refq = orc.fused_rmsnorm_silu(x[lo:hi], w, 1e-6, weight_bias=bias, fp8=True,
+                                          scale=1.0 if scale is None else scale)
+            gu.check_fp8(gq[lo:hi], refq["q"], refq["v_exact"], 0,
+                         what=f"silu e4m3 scale={scale} rows {lo}:{hi}")
+    gu.each_block(T, H, check)
 
 
 @pytest.mark.parametrize("H", SILU_H)
@@ -70,13 +76,13 @@ def test_silu_row_counts(orc, T):
     _check_silu(orc, x, synth.random_weight(T, 160))
 
 
-def test_silu_large_sampled(orc):
-    # The largest point of the B200 sweep grid, T = 399360, H = 1024, checked
-    # on sampled rows (the op is row-independent).
+def test_silu_large(orc):
+    # The largest point of the B200 sweep grid, T = 399360, H = 1024, every
+    # row.
     T, H = 399360, 1024
     gen = torch.Generator().manual_seed(3)
     x = synth.bf16_bits(torch.randn(T, H, generator=gen))
-    _check_silu(orc, x, synth.random_weight(3, H), rows=gu.sample_rows(T))
+    _check_silu(orc, x, synth.random_weight(3, H))
 
 
 def test_silu_in_place_and_strided(orc):
@@ -120,33 +126,41 @@ def _ln_allowance(x, ref, gamma, beta):
     return 2.0 ** -20 * (d * ref["rstd"][:, None] * np.abs(gamma) + np.abs(beta))
 
 
-def _check_ln(orc, x, gamma, beta, eps=1e-5, rows=None, kinds=(0, 1)):
+def _check_ln(orc, x, gamma, beta, eps=1e-5, kinds=(0, 1)):
+    """Every row: BF16 output, mean, rstd, and the FP8 codes of each kind."""
     xd = gu.dev_bf16(x)
     gd, bd = gu.dev_f32(gamma), gu.dev_f32(beta)
-    T = x.shape[0]
+    T, H = x.shape
     mean = torch.empty(T, dtype=torch.float32, device="cuda")
     rstd = torch.empty(T, dtype=torch.float32, device="cuda")
     y = crm.layernorm(xd, gd, bd, eps, mean=mean, rstd=rstd)
     torch.cuda.synchronize()
-    sel = slice(None) if rows is None else rows
-    xs = x[sel]
-    ref = orc.layernorm(xs, gamma, beta, eps)
-    xdec = orc.bf16_to_f64(xs)
-    allow = _ln_allowance(xdec, ref, gamma, beta)
-    gu.check_bf16(gu.host_bits(y)[sel], ref["v_exact"], allowance=allow, what="layernorm")
-    gu.check_rstd(rstd.cpu().numpy()[sel], ref["rstd"])
-    m = mean.cpu().numpy()[sel].astype(np.float64)
-    scale_m = np.abs(xdec).mean(axis=1)
-    assert np.all(np.abs(m - ref["mean"]) <= 2.0 ** -22 * scale_m + 1e-30), "mean"
+    yb, mb, rb = gu.host_bits(y), mean.cpu().numpy().astype(np.float64), rstd.cpu().numpy()
+    del y
+    qs = {}
     for kind in kinds:
         dt = torch.float8_e4m3fn if kind == 0 else torch.float8_e5m2
         q = torch.empty(xd.shape, dtype=dt, device="cuda")
         crm.layernorm_quant(q, xd, gd, bd, 0.04, eps)
         torch.cuda.synchronize()
-        rq = orc.layernorm(xs, gamma, beta, eps, fp8_kind=kind, scale=0.04)
-        gu.check_fp8(gu.host_u8(q)[sel], rq["q"], rq["v_exact"], kind,
-                     what=f"layernorm_quant kind={kind}",
-                     allowance=allow / float(np.float32(0.04)))
+        qs[kind] = gu.host_u8(q)
+        del q
+
+    def check(lo, hi):
+        xs = x[lo:hi]
+        ref = orc.layernorm(xs, gamma, beta, eps)
+        xdec = orc.bf16_to_f64(xs)
+        allow = _ln_allowance(xdec, ref, gamma, beta)
+        gu.check_bf16(yb[lo:hi], ref["v_exact"], allowance=allow, what=f"layernorm rows {lo}:{hi}")
+        gu.check_rstd(rb[lo:hi], ref["rstd"], what=f"rstd rows {lo}:{hi}")
+        scale_m = np.abs(xdec).mean(axis=1)
+        assert np.all(np.abs(mb[lo:hi] - ref["mean"]) <= 2.0 ** -22 * scale_m + 1e-30), "mean"
+        for kind, gq in qs.items():
+            rq = orc.layernorm(xs, gamma, beta, eps, fp8_kind=kind, scale=0.04)
+            gu.check_fp8(gq[lo:hi], rq["q"], rq["v_exact"], kind,
+                         what=f"layernorm_quant kind={kind} rows {lo}:{hi}",
+                         allowance=allow / float(np.float32(0.04)))
+    gu.each_block(T, H, check)
 
 
 # 6144: the persistent form's gamma/beta table is exactly 48 KB, which with
@@ -162,7 +176,19 @@ def test_layernorm_widths(orc, H):
 def test_layernorm_row_counts(orc, T):
     x = synth.random_rows(T + 5, T, 768)[0]
     g, b = _gamma_beta(T, 768)
-    _check_ln(orc, x, g, b, rows=None if T < 1000 else gu.sample_rows(T))
+    _check_ln(orc, x, g, b)
+
+
+def test_layernorm_large(orc):
+    # The measured LayerNorm workload, T = 16384, H = 4096, every row; the
+    # last 1024 rows carry a large common offset (300 + N(0,1)).
+    T, H = 16384, 4096
+    gen = torch.Generator().manual_seed(8)
+    v = torch.randn(T, H, generator=gen)
+    v[T - 1024:] += 300.0
+    x = synth.bf16_bits(v)
+    g, b = _gamma_beta(8, H)
+    _check_ln(orc, x, g, b)
 
 
 def test_layernorm_offset_rows(orc):

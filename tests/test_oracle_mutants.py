@@ -73,3 +73,29 @@ def test_mutant_is_caught(tmp_path, name, old, new, occ):
         except (AssertionError, ValueError, FloatingPointError, ZeroDivisionError) as e:
             caught.append(pin.__name__)
     assert caught, f"no pin catches the planted mistake {name}"
+
+
+# Planted mistakes in the epilogues that a hand-derived golden alone must
+# catch (not only the pins that compare the oracle with itself).
+GOLDEN_CAUGHT = ["quant_multiplies_scale", "e4m3_no_saturation", "ada_no_one_plus",
+                 "ada_shift_dropped", "ada_gate_from_shift", "gated_gate_from_shift",
+                 "gated_no_one_plus", "silu_exp_sign", "silu_sigmoid_only", "silu_fp8_multiplies",
+                 "ln_unbiased_var", "ln_beta_dropped", "ln_not_centred", "ln_eps_outside_root",
+                 "ln_quant_formats_swapped", "block_scale_240", "dx_sign", "eps_added_to_sum"]
+
+
+@pytest.mark.parametrize("name", GOLDEN_CAUGHT)
+def test_golden_catches_mutant(tmp_path, name):
+    old, new, occ = next((m[1], m[2], m[3]) for m in MUTANTS if m[0] == name)
+    src = oracle.source_text()
+    path = oracle.compile_variant(_mutate(src, old, new, occ), os.path.join(tmp_path, f"{name}.so"))
+    mutant = oracle.Oracle(oracle.load_path(path))
+    caught = []
+    for pin in oracle_pins.ALL_PINS:
+        if not pin.__name__.startswith("pin_golden"):
+            continue
+        try:
+            pin(mutant)
+        except (AssertionError, ValueError, FloatingPointError, ZeroDivisionError):
+            caught.append(pin.__name__)
+    assert caught, f"no hand-derived golden catches the planted mistake {name}"
