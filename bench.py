@@ -217,11 +217,14 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- GPU side --
 
-def other_kernels(dev, peak):
-    """Each remaining hot-path kernel at its own workload, launched back to
-    back over rotating input/output sets whose total is at least 2x the L2
-    size, so that no launch finds its inputs in L2; average device time per
-    launch from one pair of CUDA events around the whole loop."""
+def other_kernels(dev, peak, only=None):
+    """Each hot-path kernel at its own workload, launched back to back over
+    rotating input/output sets whose total is at least 2x the L2 size (at
+    most 64 sets: the smallest problems stay L2-resident and are reported as
+    latency), so that no launch of a large problem finds its inputs in L2;
+    average device time per launch from one pair of CUDA events around the
+    whole loop on the launching stream.  `only`: a substring; rows whose
+    name does not contain it are skipped."""
     import torch
 
     import normalization_rmsnorm_fwd_gb300 as crm
@@ -233,23 +236,38 @@ def other_kernels(dev, peak):
         return (shift + scale * torch.randn(*shape, device=dev)).to(torch.bfloat16)
 
     def add(name, make, nbytes, launches=60):
-        sets = [make() for _ in range(max(1, -(-2 * l2 // nbytes)))]
+        if only is not None and only not in name:
+            return None
+        sets = [make() for _ in range(min(64, max(1, -(-2 * l2 // nbytes))))]
         for f in sets:
             f()
         torch.cuda.synchronize()
         st = torch.cuda.current_stream()
+        n = max(launches, 2 * len(sets))
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(st)
-        for i in range(launches):
+        for i in range(n):
             sets[i % len(sets)]()
         b.record(st)
         torch.cuda.synchronize()
-        us = a.elapsed_time(b) / launches * 1e3
+        us = a.elapsed_time(b) / n * 1e3
         gbs = nbytes / us / 1e3
-        out.append({"kernel": name, "bytes": nbytes, "us": round(us, 2), "gbs": round(gbs, 1),
-                    "frac": round(gbs / peak, 4), "rotating_sets": len(sets)})
+        row = {"kernel": name, "bytes": nbytes, "us": round(us, 2), "gbs": round(gbs, 1),
+               "frac": round(gbs / peak, 4), "rotating_sets": len(sets),
+               "l2_resident": len(sets) * nbytes < 2 * l2}
+        out.append(row)
         del sets
         torch.cuda.empty_cache()
+        return row
+
+    # The fused-residual forward of the step on its own (one launch per
+    # call), the source of the roofline line.
+    def fwd_res():
+        x, r = randn(T_ROWS, H), randn(T_ROWS, H)
+        w = randn(H, scale=0.1, shift=1.0)
+        y, hn, rs = torch.empty_like(x), torch.empty_like(x), torch.empty(T_ROWS, device=dev)
+        return lambda: crm.rmsnorm_fwd(x, w, 1e-6, residual=r, y=y, rstd=rs, h_new=hn)
+    add("rmsnorm_fwd fused residual alone T=16384 H=4096", fwd_res, FWD_BYTES)
 
     sc = torch.tensor([0.04], device=dev)
 
@@ -270,12 +288,49 @@ def other_kernels(dev, peak):
         return lambda: crm.rmsnorm_fwd(x, w, y=y, rstd=r)
     add("rmsnorm_fwd plain T=16384 H=4096", plain, 2 * 16384 * 4096 * 2 + 4096 * 2 + 16384 * 4)
 
-    def zc():
-        x, w = randn(16384, 5120, scale=4.0), 0.02 * torch.randn(5120, device=dev)
-        y, r = torch.empty_like(x), torch.empty(16384, device=dev)
-        return lambda: crm.rmsnorm_fwd(x, w, weight_bias=1.0, y=y, rstd=r)
-    add("rmsnorm_fwd FP32 zero-centred weight T=16384 H=5120", zc,
-        2 * 16384 * 5120 * 2 + 5120 * 4 + 16384 * 4)
+    # Zero-centred FP32 weight (effective 1 + w), H = 5120, x ~ 4 N(0,1),
+    # forward and backward at every token count of the workload.
+    Hz = 5120
+    for Tz in (1, 7, 128, 1024, 1025, 4096, 16384):
+        def zc_fwd(Tz=Tz):
+            x, w = randn(Tz, Hz, scale=4.0), 0.02 * torch.randn(Hz, device=dev)
+            y, r = torch.empty_like(x), torch.empty(Tz, device=dev)
+            return lambda: crm.rmsnorm_fwd(x, w, weight_bias=1.0, y=y, rstd=r)
+        add(f"rmsnorm_fwd FP32 zero-centred weight T={Tz} H=5120", zc_fwd,
+            2 * Tz * Hz * 2 + Hz * 4 + Tz * 4)
+
+        def zc_bwd(Tz=Tz):
+            g, x = randn(Tz, Hz), randn(Tz, Hz, scale=4.0)
+            w = 0.02 * torch.randn(Hz, device=dev)
+            rstd = 0.25 * (torch.rand(Tz, device=dev) + 0.5)
+            dx, dw = torch.empty_like(x), torch.empty(Hz, device=dev)
+            ws = crm.rmsnorm_bwd_workspace(Tz, Hz, dev)
+            return lambda: crm.rmsnorm_bwd(g, x, w, rstd, 1.0, dx=dx, dw=dw, workspace=ws)
+        add(f"rmsnorm_bwd FP32 zero-centred weight T={Tz} H=5120 (dx + dw, two launches)", zc_bwd,
+            3 * Tz * Hz * 2 + Tz * 4 + 2 * Hz * 4)
+
+    # The [2048, 32, 128] row-strided view of a [2048, 32, 256] buffer:
+    # 65536 rows of H = 128, row stride 256, FP32 zero-centred weight.
+    Th, Hh = 2048 * 32, 128
+
+    def heads_fwd():
+        buf = randn(2048, 32, 256)
+        w = 0.02 * torch.randn(Hh, device=dev)
+        y, r = torch.empty(2048, 32, Hh, dtype=torch.bfloat16, device=dev), torch.empty(2048, 32, device=dev)
+        return lambda: crm.rmsnorm_fwd(buf[..., :Hh], w, weight_bias=1.0, y=y, rstd=r)
+    add("rmsnorm_fwd strided heads [2048,32,128] of [2048,32,256]", heads_fwd,
+        2 * Th * Hh * 2 + Hh * 4 + Th * 4)
+
+    def heads_bwd():
+        buf, gbuf = randn(2048, 32, 256), randn(2048, 32, 256)
+        w = 0.02 * torch.randn(Hh, device=dev)
+        rstd = torch.rand(2048, 32, device=dev) + 0.5
+        dx, dw = torch.empty(2048, 32, Hh, dtype=torch.bfloat16, device=dev), torch.empty(Hh, device=dev)
+        ws = crm.rmsnorm_bwd_workspace(Th, Hh, dev)
+        return lambda: crm.rmsnorm_bwd(gbuf[..., Hh:], buf[..., :Hh], w, rstd, 1.0, dx=dx, dw=dw,
+                                       workspace=ws)
+    add("rmsnorm_bwd strided heads [2048,32,128] of [2048,32,256] (dx + dw, two launches)",
+        heads_bwd, 3 * Th * Hh * 2 + Th * 4 + 2 * Hh * 4)
 
     def quant():
         x, r, w = randn(8192, 8192), randn(8192, 8192), randn(8192, scale=0.1, shift=1.0)
@@ -347,6 +402,145 @@ def other_kernels(dev, peak):
     add("layernorm bf16 T=16384 H=4096", ln(False), 16384 * 4096 * 4 + 4096 * 8)
     add("layernorm_quant e4m3 T=16384 H=4096", ln(True), 16384 * 4096 * 3 + 4096 * 8 + 4)
     return out
+
+
+def split_copy(pairs, streams, waits, done):
+    """Copy every (dst, src) pair, each split into len(streams) contiguous
+    chunks, chunk i on streams[i] (one cudaMemcpyAsync per chunk) after
+    that stream has waited for the events in `waits`; done[i] is recorded
+    on streams[i] after its chunks."""
+    import torch
+    k = len(streams)
+    for i, st in enumerate(streams):
+        with torch.cuda.stream(st):
+            for e in waits:
+                st.wait_event(e)
+            for dst, src in pairs:
+                n = dst.numel()
+                a, b = n * i // k, n * (i + 1) // k
+                if b > a:
+                    dst.view(-1)[a:b].copy_(src.view(-1)[a:b], non_blocking=True)
+            done[i].record(st)
+
+
+def copy_ceiling(dev, h_in, d_in, d_out, h_out, reps=5):
+    """The host link's ceiling for the end-to-end leg's bytes: the time of
+    the pinned host->device copies of a step's inputs and the device->host
+    copies of its outputs, each direction alone and both at once, with every
+    tensor split over 1, 2 or 4 streams.  Returns the rows and the stream
+    count with the shortest both-directions time."""
+    import torch
+    rows = []
+    best = None
+    nin = sum(t.numel() * t.element_size() for t in h_in)
+    nout = sum(t.numel() * t.element_size() for t in h_out)
+    for k in (1, 2, 4):
+        sin = [torch.cuda.Stream(dev) for _ in range(k)]
+        sout = [torch.cuda.Stream(dev) for _ in range(k)]
+        ev = [torch.cuda.Event() for _ in range(k)]
+
+        def timed(do_in, do_out):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(reps):
+                if do_in:
+                    split_copy(list(zip(d_in, h_in)), sin, [], ev)
+                if do_out:
+                    split_copy(list(zip(h_out, d_out)), sout, [], ev)
+            torch.cuda.synchronize()
+            return (time.perf_counter() - t0) / reps * 1e3
+        timed(True, True)
+        ms_in, ms_out, ms_both = timed(True, False), timed(False, True), timed(True, True)
+        row = {"streams_per_direction": k, "h2d_ms": round(ms_in, 3), "d2h_ms": round(ms_out, 3),
+               "both_ms": round(ms_both, 3), "h2d_gbs": round(nin / ms_in / 1e6, 1),
+               "d2h_gbs": round(nout / ms_out / 1e6, 1),
+               "both_gbs": round((nin + nout) / ms_both / 1e6, 1)}
+        rows.append(row)
+        if best is None or ms_both < best[1]:
+            best = (k, ms_both)
+    return rows, best[0]
+
+
+def run_e2e(args, world, dev, x, r, g, w, y, rs0, dw, ws):
+    """End to end through the public API with host buffers: every step
+    copies its inputs in from pinned host memory, runs both calls and copies
+    every output back, all inside the timing.  Steps are pipelined over two
+    buffer sets (copy-in streams, a compute stream, copy-out streams,
+    ordered by events), so one step's copies overlap its neighbours' work;
+    each tensor's copy is split over the number of streams per direction
+    that gave the host link's best measured rate."""
+    import torch
+
+    import normalization_rmsnorm_fwd_gb300 as crm
+    pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    hx, hr, hg = pin(x), pin(r), pin(g)
+    hx.copy_(x); hr.copy_(r); hg.copy_(g)
+    h2d = 3 * T_ROWS * H * 2
+    d2h = 3 * T_ROWS * H * 2 + T_ROWS * 4 + H * 4
+    sets = []
+    for _ in range(2):
+        d = {k: torch.empty_like(v) for k, v in (("x", x), ("r", r), ("g", g), ("y", y),
+                                                  ("hn", y), ("dx", y))}
+        d["rs"] = torch.empty_like(rs0)
+        d["dw"] = torch.empty_like(dw)
+        d["ws"] = torch.empty_like(ws)
+        d["out"] = {k: pin(d[k]) for k in ("y", "hn", "dx", "rs", "dw")}
+        sets.append(d)
+    keys = ("y", "hn", "dx", "rs", "dw")
+    ceiling, k = copy_ceiling(dev, [hx, hr, hg], [sets[0]["x"], sets[0]["r"], sets[0]["g"]],
+                              [sets[0][q] for q in keys], [sets[0]["out"][q] for q in keys])
+    s_in = [torch.cuda.Stream(dev) for _ in range(k)]
+    s_out = [torch.cuda.Stream(dev) for _ in range(k)]
+    s_cmp = torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()
+    in_done = [[ev() for _ in range(k)] for _ in range(2)]
+    cmp_done = [ev(), ev()]
+    out_done = [[ev() for _ in range(k)] for _ in range(2)]
+
+    def e2e_step(step):
+        b = step % 2
+        d = sets[b]
+        # set b's previous step must have left the device before its inputs
+        # are overwritten
+        split_copy([(d["x"], hx), (d["r"], hr), (d["g"], hg)], s_in,
+                   out_done[b] if step >= 2 else [], in_done[b])
+        with torch.cuda.stream(s_cmp):
+            for e in in_done[b]:
+                s_cmp.wait_event(e)
+            crm.rmsnorm_fwd(d["x"], w, 1e-6, residual=d["r"], y=d["y"], rstd=d["rs"],
+                            h_new=d["hn"])
+            crm.rmsnorm_bwd(d["g"], d["hn"], w, d["rs"], dx=d["dx"], dw=d["dw"],
+                            workspace=d["ws"])
+            cmp_done[b].record(s_cmp)
+        split_copy([(d["out"][q], d[q]) for q in keys], s_out, [cmp_done[b]], out_done[b])
+
+    for step in range(4):
+        e2e_step(step)
+    torch.cuda.synchronize()
+    ne = max(4, min(args.steps, 20))
+    a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    a_ev.record(s_in[0])
+    for st in s_in[1:] + s_out + [s_cmp]:
+        st.wait_stream(s_in[0])
+    for step in range(ne):
+        e2e_step(step)
+    for st in s_in + s_out[1:] + [s_cmp]:
+        s_out[0].wait_stream(st)
+    b_ev.record(s_out[0])
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a_ev.elapsed_time(b_ev) / ne, world, dev)
+    best = min(ceiling, key=lambda c: c["both_ms"])
+    return {"value": world * STEP_BYTES / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": e2e_ms,
+            "pipelining": f"two buffer sets; {k} copy-in and {k} copy-out streams per direction, "
+                          "one compute stream",
+            "copy_ceiling": {"rows": ceiling, "best_both_ms": best["both_ms"],
+                             "frac_of_copy_ceiling": round(best["both_ms"] / e2e_ms, 4),
+                             "note": "pinned host<->device copies of one step's bytes alone, "
+                                     "without the kernels (host wall clock around synchronised "
+                                     "copies)"}}
 
 
 def run_ours(args):
@@ -443,74 +637,17 @@ def run_ours(args):
     # the whole loop's, divided by the steps.
     e2e = None
     if rank == 0 or world > 1:
-        pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-        hx, hr, hg = pin(x), pin(r), pin(g)
-        hx.copy_(x); hr.copy_(r); hg.copy_(g)
-        h2d = 3 * T_ROWS * H * 2
-        d2h = 3 * T_ROWS * H * 2 + T_ROWS * 4 + H * 4
-        sets = []
-        for _ in range(2):
-            d = {k: torch.empty_like(v) for k, v in (("x", x), ("r", r), ("g", g), ("y", y),
-                                                      ("hn", y), ("dx", y))}
-            d["rs"] = torch.empty_like(rs[0])
-            d["dw"] = torch.empty_like(dw)
-            d["ws"] = torch.empty_like(ws)
-            d["out"] = {k: pin(d[k]) for k in ("y", "hn", "dx", "rs", "dw")}
-            sets.append(d)
-        s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-        ev = lambda: torch.cuda.Event()
-        in_done = [ev(), ev()]
-        cmp_done = [ev(), ev()]
-        out_done = [ev(), ev()]
-
-        def e2e_step(k):
-            b = k % 2
-            d = sets[b]
-            with torch.cuda.stream(s_in):
-                if k >= 2:
-                    s_in.wait_event(out_done[b])          # set b's previous step is finished
-                d["x"].copy_(hx, non_blocking=True)
-                d["r"].copy_(hr, non_blocking=True)
-                d["g"].copy_(hg, non_blocking=True)
-                in_done[b].record(s_in)
-            with torch.cuda.stream(s_cmp):
-                s_cmp.wait_event(in_done[b])
-                crm.rmsnorm_fwd(d["x"], w, 1e-6, residual=d["r"], y=d["y"], rstd=d["rs"],
-                                h_new=d["hn"])
-                crm.rmsnorm_bwd(d["g"], d["hn"], w, d["rs"], dx=d["dx"], dw=d["dw"],
-                                workspace=d["ws"])
-                cmp_done[b].record(s_cmp)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(cmp_done[b])
-                for key, host in d["out"].items():
-                    host.copy_(d[key], non_blocking=True)
-                out_done[b].record(s_out)
-
-        for k in range(4):
-            e2e_step(k)
-        torch.cuda.synchronize()
-        ne = max(4, min(args.steps, 20))
-        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        barrier(world)
-        a_ev.record(s_in)
-        for k in range(ne):
-            e2e_step(k)
-        s_out.wait_stream(s_in)
-        s_out.wait_stream(s_cmp)
-        b_ev.record(s_out)
-        torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(a_ev.elapsed_time(b_ev) / ne, world, dev)
-        e2e = {"value": world * STEP_BYTES / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_ms,
-               "pipelining": "two buffer sets; copy-in, compute and copy-out streams"}
-        del hx, hr, hg, sets
+        e2e = run_e2e(args, world, dev, x, r, g, w, y, rs[0], dw, ws)
+        torch.cuda.empty_cache()
 
     per_kernel = None
-    if rank == 0 and not args.no_extra:
+    if rank == 0:
         del x, r, g, y, dx, hn, rs
         torch.cuda.empty_cache()
-        per_kernel = other_kernels(dev, peak)
+        # The standalone forward always runs: it is the roofline's source.
+        per_kernel = other_kernels(dev, peak, only=None if not args.no_extra else "alone")
+    standalone = {row["kernel"]: row for row in per_kernel or []}
+    fwd_alone = standalone.get("rmsnorm_fwd fused residual alone T=16384 H=4096")
 
     if rank != 0:
         if world > 1:
@@ -518,6 +655,12 @@ def run_ours(args):
             dist.destroy_process_group()
         return
 
+    # Roofline of the dominant kernel: the fused-residual forward timed on its
+    # own (back-to-back launches over inputs larger than L2, events around
+    # the loop); the event-split step loop is kept as `in_step`.
+    fwd_in_step_us = fwd_us
+    if fwd_alone is not None:
+        fwd_us = fwd_alone["us"]
     fwd_gbs = FWD_BYTES / fwd_us / 1e3
     bwd_gbs = BWD_BYTES / bwd_us / 1e3
     value = world * STEP_BYTES / (ms_step * 1e-3) / 1e9
@@ -537,6 +680,9 @@ def run_ours(args):
                      "achieved": round(fwd_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(fwd_gbs / peak, 4), "peak_kind": peak_kind + " hbm_gbs",
                      "bytes_per_launch": FWD_BYTES, "us_per_launch": round(fwd_us, 2),
+                     "timing": ("standalone: back-to-back launches, events around the loop"
+                                if fwd_alone is not None else "event-split step loop"),
+                     "in_step_us": round(fwd_in_step_us, 2),
                      "traffic": ncu_traffic("rmsnorm_fwd")},
         "backward": {"achieved": round(bwd_gbs, 1), "frac": round(bwd_gbs / peak, 4),
                      "bytes_per_call": BWD_BYTES, "us_per_call": round(bwd_us, 2),
@@ -556,6 +702,23 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+def run_kernel_rows(args):
+    """Only the per-kernel rows matching --kernel, on rank 0 (profiling)."""
+    import torch
+
+    from normalization_rmsnorm_fwd_gb300 import _abi
+    rank, local_rank, _ = dist_env()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    _abi.load()
+    peak, _ = measured_peaks()
+    rows = other_kernels(dev, peak, only=args.kernel)
+    print(json.dumps({"impl": "ours", "mode": "kernel rows", "filter": args.kernel,
+                      "per_kernel": rows}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -563,12 +726,18 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--no-extra", action="store_true", help="skip the per-kernel table")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the per-kernel table (but for the standalone forward)")
+    ap.add_argument("--kernel", default=None,
+                    help="only run the per-kernel rows whose name contains this text "
+                         "(no timed step, no e2e, no CPU baseline; for profiling one kernel)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.kernel is not None:
+        run_kernel_rows(args)
     else:
         run_ours(args)
 
