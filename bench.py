@@ -383,8 +383,8 @@ def other_kernels(dev, peak, only=None):
                             device=dev)
             return lambda: crm.fused_rmsnorm_silu(x, w, out=o)
         return make
-    for Ts, H in ((399360, 1024), (399360, 128)):
-        add(f"fused_rmsnorm_silu bf16 T={Ts} H={H}", silu(Ts, H, False), Ts * H * 4 + H * 2)
+    for Ts, Hs in ((399360, 1024), (399360, 128)):
+        add(f"fused_rmsnorm_silu bf16 T={Ts} H={Hs}", silu(Ts, Hs, False), Ts * Hs * 4 + Hs * 2)
     add("fused_rmsnorm_silu e4m3 T=399360 H=1024", silu(399360, 1024, True),
         399360 * 1024 * 3 + 1024 * 2)
 

@@ -52,6 +52,12 @@
 
 #include <cuda_runtime_api.h>
 
+/* The library is built with hidden symbols; only these declarations are
+ * exported. */
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -183,8 +189,8 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t rows, int64_t H, int device,
  * calls on a device share the array: calls that overlap on the GPU (other
  * streams or host threads) race and must be serialised.  The scratch needs
  * no zeroing.  Problems whose workspace (rmsnorm_bwd_workspace_bytes) exceeds
- * 16 MiB -- on a 152-SM GB300, H above about 13,700 -- return
- * CRMSN_ERR_SCRATCH_LIMIT without launching anything.
+ * 16 MiB return CRMSN_ERR_SCRATCH_LIMIT without launching anything; on a
+ * 152-SM GB300 every H fits (the workspace stays below 12 MB).
  */
 crmsn_status rmsnorm_bwd_noalloc(const void *g, int64_t ldg,
                                  const void *x, int64_t ldx,
@@ -351,5 +357,9 @@ const char *crmsn_status_str(crmsn_status status);
 
 #ifdef __cplusplus
 }
+#endif
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
 #endif
 #endif /* CRMSNORM_H */

@@ -23,8 +23,12 @@ OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libcrmsnorm.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# Hidden symbols: the shared library exports only the C ABI of crmsnorm.h,
+# so its internal template statics (launch caches) are never merged with
+# another library's in the same process.
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", *ARCH, "-Xcompiler", "-fPIC",
-              "-Xcompiler", "-Wall", "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
+              "-Xcompiler", "-fvisibility=hidden", "-Xcompiler", "-Wall",
+              "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
 
 
 def _nvcc() -> str:

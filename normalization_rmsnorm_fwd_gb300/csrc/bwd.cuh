@@ -56,7 +56,7 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
 // Rows summed plainly per column before each compensated fold.
-constexpr int kDwBlock = 8;
+constexpr int kDwBlock = 16;
 
 // VEC BF16 values from a 16-byte (4-byte) aligned shared-memory slot in one
 // access.
@@ -86,19 +86,6 @@ __device__ __forceinline__ void ld_smem_f2(const float *p, F2 (&f)[VEC / 2])
         const float2 a = *reinterpret_cast<const float2 *>(p);
         f[0] = f2(a.x, a.y);
     }
-}
-
-// Exact FP32 products of the two BF16 pairs packed in g and x (low halves,
-// high halves): one mixed-precision FMA (BF16 operands, FP32 addend and
-// result, sm_100 and later) per product, no unpacking.  A product of two
-// BF16 values has at most 16 significant bits, so it is exact in FP32.
-__device__ __forceinline__ F2 mul_bf16x2(uint32_t g, uint32_t x)
-{
-    float lo, hi;
-    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %2;\n\tmov.b32 {b0, b1}, %3;\n\t"
-        "fma.rn.f32.bf16 %0, a0, b0, %4;\n\tfma.rn.f32.bf16 %1, a1, b1, %4;\n}"
-        : "=f"(lo), "=f"(hi) : "r"(g), "r"(x), "f"(0.f));
-    return f2(lo, hi);
 }
 
 // Bytes of one ring stage: NT tensors x VPT vectors per thread.
@@ -131,7 +118,7 @@ k_rmsnorm_bwd(const BwdParams p)
     const int nthr = blockDim.x;
     const int tpr = p.tpr;
     const int rpc = p.rpc;
-    const int grp = threadIdx.x / tpr;
+    const int grp = row_group(tpr, p.rpc);
     const int lane = threadIdx.x - grp * tpr;
     const int nvec = p.H / VEC;
     const int64_t r0 = (int64_t)blockIdx.x * p.T / p.nchunk;
@@ -403,7 +390,7 @@ k_rmsnorm_bwd(const BwdParams p)
         };
 
         // The dw terms of a row are taken in its sum phase, from the exact
-        // products g*x; block sums fold after every kDwBlock rows as before.
+        // products g*x; block sums fold after every kDwBlock rows.
         cp_async_wait<D - 1>();              // row 0 landed
         {
             const F2 rs2 = f2(rs_of(0, 0));
@@ -445,7 +432,6 @@ k_rmsnorm_bwd(const BwdParams p)
                 if (live) dx_vec(false, dxrow, st, k, we, rs2, nc3);
             }
             publish(it + 1, dot2);
-            if ((it + 2) % kDwBlock == 0) fold();
             rs_advance(it);
             t += rpc;
             dxrow += (int64_t)rpc * p.lddx;
@@ -453,9 +439,19 @@ k_rmsnorm_bwd(const BwdParams p)
             __syncthreads();
             tot = group_total(it + 1);
         };
+        // Steps in blocks that end where the block sums fold (after the step
+        // with (it + 2) % kDwBlock == 0), so the fold never sits inside the
+        // per-row body; the last two steps check liveness.
         int64_t it = 0;
-        for (; it + 2 < iters; ++it) step(it, false);
-        for (; it < iters; ++it) step(it, true);
+        const int64_t nfast = iters > 2 ? iters - 2 : 0;
+        while (it < iters) {
+            int64_t stop = it + (kDwBlock - (it + 2) % kDwBlock);
+            if (stop > iters) stop = iters;
+            const int64_t fstop = stop < nfast ? stop : nfast;
+            for (; it < fstop; ++it) step(it, false);
+            for (; it < stop; ++it) step(it, true);
+            if ((it + 1) % kDwBlock == 0) fold();
+        }
     } else {
         int64_t t = r0 + grp;                // row of iteration it
         uint16_t *dxrow = p.dx + t * p.lddx + (int64_t)lane * VEC;
@@ -545,91 +541,145 @@ inline size_t bwd_smem_bytes(bool gres, int vec, int vpt, int threads, int rpc, 
            ((size_t)vpt * (threads / rpc) * vec + (rpc > 1 ? (size_t)rpc * H * 2 : 0)) * sizeof(float);
 }
 
-// Launch of one instantiation: picks the chunk count from the occupancy of
-// this kernel (at most kBwdMaxCtasPerSm CTAs per SM, at most one chunk per
-// row group), launches it and returns the chunk count used.
-template <bool W32, bool GRES, int VEC, int VPT, bool SUB, int D>
-cudaError_t launch_bwd_inst(BwdParams p, int sms, int *nchunk_out, cudaStream_t s)
-{
-    const int threads = p.tpr * p.rpc;
-    const size_t smem = bwd_smem_bytes(GRES, VEC, VPT, threads, p.rpc, p.H, D);
-    auto kern = k_rmsnorm_bwd<W32, GRES, VEC, VPT, SUB, D>;
-    static std::atomic<int> opted[kOptInDevices];
-    cudaError_t e = opt_in_smem(kern, smem, opted);
-    if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    if (per_sm > kBwdMaxCtasPerSm) per_sm = kBwdMaxCtasPerSm;
-    const int64_t by_rows = (p.T + p.rpc - 1) / p.rpc;
-    const int64_t cap = (int64_t)per_sm * sms;
-    p.nchunk = (int)(by_rows < cap ? by_rows : cap);
-    *nchunk_out = p.nchunk;
-    return launch_pdl(kern, dim3((unsigned)p.nchunk), dim3(threads), smem, s, p);
-}
+// The most shared memory a CTA may ask for, and the most the backward's
+// CTAs on one SM are given together when a depth is chosen (measured: two
+// CTAs taking 226 KB with g_residual at H = 4096 ran at 103.7 us, two of
+// 89 KB at 94.7 us; 200 KB at H = 5120 was still the fastest).
+constexpr size_t kBwdSmemMax = 227 * 1024;
+constexpr size_t kBwdSmemPerSm = 208 * 1024;
 
-// Dispatch over layouts (SUB groups with VPT 1|2; multi-warp groups with VPT
-// 1|2|4 for 16-byte vectors, 1|2|4|8|16 for 4-byte vectors) and the prefetch
-// depth (3 rows ahead when four stages fit in shared memory, else 1).
-template <bool W32, bool GRES, int VEC, int D>
-cudaError_t launch_bwd_vd(const BwdParams &p, const Layout &L, int sms, int *nc, cudaStream_t s)
+// One instantiation: its residency (CTAs per SM for a block size and
+// shared-memory size, computed once per key and remembered) and its launch
+// with a chunk count of at most per_sm x SMs (and at most one chunk per row
+// group).
+template <bool W32, bool GRES, int VEC, int VPT, bool SUB, int D>
+struct BwdInst {
+    static constexpr auto kern = k_rmsnorm_bwd<W32, GRES, VEC, VPT, SUB, D>;
+
+    static cudaError_t occupancy(const BwdParams &p, int *per_sm)
+    {
+        const int threads = p.tpr * p.rpc;
+        const size_t smem = bwd_smem_bytes(GRES, VEC, VPT, threads, p.rpc, p.H, D);
+        static std::atomic<int> opted[kOptInDevices];
+        cudaError_t e = opt_in_smem(kern, smem, opted);
+        if (e != cudaSuccess) return e;
+        // threads << 40 | shared-memory bytes << 8 | CTAs per SM
+        static std::atomic<long long> cached{0};
+        const long long key = ((long long)threads << 40) | ((long long)smem << 8);
+        const long long c = cached.load(std::memory_order_relaxed);
+        if ((c & ~0xffLL) == key && (c & 0xff) > 0) {
+            *per_sm = (int)(c & 0xff);
+            return cudaSuccess;
+        }
+        int n = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem);
+        if (e != cudaSuccess) return e;
+        if (n > 255) n = 255;
+        if (n > 0) cached.store(key | n, std::memory_order_relaxed);
+        *per_sm = n;
+        return cudaSuccess;
+    }
+
+    static cudaError_t launch(BwdParams p, int per_sm, int sms, int *nchunk_out, cudaStream_t s)
+    {
+        const int threads = p.tpr * p.rpc;
+        const size_t smem = bwd_smem_bytes(GRES, VEC, VPT, threads, p.rpc, p.H, D);
+        const int64_t by_rows = (p.T + p.rpc - 1) / p.rpc;
+        const int64_t cap = (int64_t)per_sm * sms;
+        p.nchunk = (int)(by_rows < cap ? by_rows : cap);
+        *nchunk_out = p.nchunk;
+        return launch_pdl(kern, dim3((unsigned)p.nchunk), dim3(threads), smem, s, p);
+    }
+};
+
+// Calls f(BwdInst<...>{}) for the instantiation of a layout (SUB groups with
+// VPT 1|2; multi-warp groups with VPT 1|2|4 for 16-byte vectors, 1|2|4|8|16
+// for 4-byte vectors; the unpipelined D = 0 form only for 32 elements per
+// thread).
+template <bool W32, bool GRES, int VEC, int D, typename F>
+cudaError_t with_bwd_inst(const Layout &L, F &&f)
 {
+    constexpr int V32 = 32 / VEC;
     if constexpr (D == 0) {
-        // Only the widest rows (32 elements per thread) need the unpipelined form.
-        if (!L.sub && L.vpt == 32 / VEC) return launch_bwd_inst<W32, GRES, VEC, 32 / VEC, false, 0>(p, sms, nc, s);
+        if (!L.sub && L.vpt == V32) return f(BwdInst<W32, GRES, VEC, V32, false, 0>{});
+        return cudaErrorInvalidConfiguration;
+    } else {
+        if (L.sub) {
+            if (L.vpt == 1) return f(BwdInst<W32, GRES, VEC, 1, true, D>{});
+            if (L.vpt == 2) return f(BwdInst<W32, GRES, VEC, 2, true, D>{});
+        } else {
+            if (L.vpt == 1) return f(BwdInst<W32, GRES, VEC, 1, false, D>{});
+            if (L.vpt == 2) return f(BwdInst<W32, GRES, VEC, 2, false, D>{});
+            if (L.vpt == 4) return f(BwdInst<W32, GRES, VEC, 4, false, D>{});
+            if constexpr (VEC == 2) {
+                if (L.vpt == 8) return f(BwdInst<W32, GRES, VEC, 8, false, D>{});
+                if (L.vpt == 16) return f(BwdInst<W32, GRES, VEC, 16, false, D>{});
+            }
+        }
         return cudaErrorInvalidConfiguration;
     }
-    if (L.sub) {
-        if (L.vpt == 1) return launch_bwd_inst<W32, GRES, VEC, 1, true, D>(p, sms, nc, s);
-        if (L.vpt == 2) return launch_bwd_inst<W32, GRES, VEC, 2, true, D>(p, sms, nc, s);
-    } else {
-        if (L.vpt == 1) return launch_bwd_inst<W32, GRES, VEC, 1, false, D>(p, sms, nc, s);
-        if (L.vpt == 2) return launch_bwd_inst<W32, GRES, VEC, 2, false, D>(p, sms, nc, s);
-        if (L.vpt == 4) return launch_bwd_inst<W32, GRES, VEC, 4, false, D>(p, sms, nc, s);
-        if constexpr (VEC == 2) {
-            if (L.vpt == 8) return launch_bwd_inst<W32, GRES, VEC, 8, false, D>(p, sms, nc, s);
-            if (L.vpt == 16) return launch_bwd_inst<W32, GRES, VEC, 16, false, D>(p, sms, nc, s);
-        }
-    }
-    return cudaErrorInvalidConfiguration;
 }
 
-// Dynamic shared memory a backward CTA may use (the SM has 228 KB).
-constexpr size_t kBwdSmemBudget = 200 * 1024;
+template <bool W32, bool GRES, int VEC, typename F>
+cudaError_t with_bwd_depth(int D, const Layout &L, F &&f)
+{
+    switch (D) {
+        case 3: return with_bwd_inst<W32, GRES, VEC, 3>(L, f);
+        case 2: return with_bwd_inst<W32, GRES, VEC, 2>(L, f);
+        case 1: return with_bwd_inst<W32, GRES, VEC, 1>(L, f);
+        default: return with_bwd_inst<W32, GRES, VEC, 0>(L, f);
+    }
+}
 
-// Prefetch depth: 3 rows ahead when four stages fit the shared-memory
-// budget, else 2, else 1, else none (only rows of 32 elements per thread at
-// H close to the maximum).
-template <bool W32>
-cudaError_t launch_bwd_weight(const BwdParams &p, bool gres, const Layout &L, int sms, int *nc,
-                              cudaStream_t s)
+// Prefetch depth and residency: among the depths whose ring fits a CTA's
+// shared memory, the one with the most rows in flight per SM (CTAs per SM --
+// capped at bwd_max_ctas_per_sm(H) and at what kBwdSmemPerSm holds --
+// times the depth), the larger CTA count on a tie; D = 0 (no ring) only
+// when no ring fits.
+template <bool W32, bool GRES, int VEC>
+cudaError_t launch_bwd_vec(const BwdParams &p, const Layout &L, int sms, int *nc, cudaStream_t s)
 {
     const int threads = p.tpr * p.rpc;
-    auto fits = [&](int d) {
-        return bwd_smem_bytes(gres, L.vec, L.vpt, threads, p.rpc, p.H, d) <= kBwdSmemBudget;
-    };
-    const int D = fits(3) ? 3 : (fits(2) ? 2 : (fits(1) ? 1 : 0));
-    if (L.vec == 8) {
-        if (gres) return D == 3 ? launch_bwd_vd<W32, true, 8, 3>(p, L, sms, nc, s)
-                       : D == 2 ? launch_bwd_vd<W32, true, 8, 2>(p, L, sms, nc, s)
-                       : D == 1 ? launch_bwd_vd<W32, true, 8, 1>(p, L, sms, nc, s)
-                                : launch_bwd_vd<W32, true, 8, 0>(p, L, sms, nc, s);
-        return D == 3 ? launch_bwd_vd<W32, false, 8, 3>(p, L, sms, nc, s)
-             : D == 2 ? launch_bwd_vd<W32, false, 8, 2>(p, L, sms, nc, s)
-             : D == 1 ? launch_bwd_vd<W32, false, 8, 1>(p, L, sms, nc, s)
-                      : launch_bwd_vd<W32, false, 8, 0>(p, L, sms, nc, s);
+    const int cap = bwd_max_ctas_per_sm(p.H);
+    int best_d = 0, best_n = 1;
+    long best_score = -1;
+    for (int d = 3; d >= 1; --d) {
+        const size_t smem = bwd_smem_bytes(GRES, VEC, L.vpt, threads, p.rpc, p.H, d);
+        if (smem > kBwdSmemMax) continue;
+        int n = 0;
+        cudaError_t e = with_bwd_depth<W32, GRES, VEC>(d, L, [&](auto inst) {
+            return decltype(inst)::occupancy(p, &n);
+        });
+        if (e != cudaSuccess) return e;
+        if (n > cap) n = cap;
+        const int by_budget = (int)(kBwdSmemPerSm / (smem + 1024));
+        if (n > by_budget) n = by_budget > 0 ? by_budget : 1;
+        if (n < 1) continue;
+        const long score = (long)n * d * 16 + n;
+        if (score > best_score) {
+            best_score = score;
+            best_d = d;
+            best_n = n;
+        }
     }
-    if (L.vec == 2) {
-        if (gres) return D == 3 ? launch_bwd_vd<W32, true, 2, 3>(p, L, sms, nc, s)
-                       : D == 2 ? launch_bwd_vd<W32, true, 2, 2>(p, L, sms, nc, s)
-                       : D == 1 ? launch_bwd_vd<W32, true, 2, 1>(p, L, sms, nc, s)
-                                : launch_bwd_vd<W32, true, 2, 0>(p, L, sms, nc, s);
-        return D == 3 ? launch_bwd_vd<W32, false, 2, 3>(p, L, sms, nc, s)
-             : D == 2 ? launch_bwd_vd<W32, false, 2, 2>(p, L, sms, nc, s)
-             : D == 1 ? launch_bwd_vd<W32, false, 2, 1>(p, L, sms, nc, s)
-                      : launch_bwd_vd<W32, false, 2, 0>(p, L, sms, nc, s);
+    if (best_score < 0) {
+        cudaError_t e = with_bwd_depth<W32, GRES, VEC>(0, L, [&](auto inst) {
+            return decltype(inst)::occupancy(p, &best_n);
+        });
+        if (e != cudaSuccess) return e;
+        if (best_n < 1) return cudaErrorInvalidConfiguration;
+        if (best_n > cap) best_n = cap;
     }
+    return with_bwd_depth<W32, GRES, VEC>(best_d, L, [&](auto inst) {
+        return decltype(inst)::launch(p, best_n, sms, nc, s);
+    });
+}
+
+template <bool W32, bool GRES>
+cudaError_t launch_bwd_weight(const BwdParams &p, const Layout &L, int sms, int *nc, cudaStream_t s)
+{
+    if (L.vec == 8) return launch_bwd_vec<W32, GRES, 8>(p, L, sms, nc, s);
+    if (L.vec == 2) return launch_bwd_vec<W32, GRES, 2>(p, L, sms, nc, s);
     return cudaErrorInvalidConfiguration;
 }
 

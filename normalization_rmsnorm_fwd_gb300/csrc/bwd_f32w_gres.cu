@@ -1,0 +1,12 @@
+// bwd_f32w_gres.cu -- backward instantiations for an FP32 weight, with g_residual.
+#include "bwd.cuh"
+
+namespace crmsn {
+
+cudaError_t launch_bwd_f32w_gres(const BwdParams &p, const Layout &L, int sms, int *nchunk,
+                                 cudaStream_t s)
+{
+    return launch_bwd_weight<true, true>(p, L, sms, nchunk, s);
+}
+
+}  // namespace crmsn

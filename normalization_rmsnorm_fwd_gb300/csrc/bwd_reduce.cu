@@ -63,8 +63,10 @@ cudaError_t launch_bwd(BwdParams p, bool w32, bool gres, const Layout &L, int sm
                        cudaStream_t s)
 {
     int nchunk = 0;
-    cudaError_t e = w32 ? launch_bwd_f32w(p, gres, L, sms, &nchunk, s)
-                        : launch_bwd_bf16w(p, gres, L, sms, &nchunk, s);
+    cudaError_t e = w32 ? (gres ? launch_bwd_f32w_gres(p, L, sms, &nchunk, s)
+                                : launch_bwd_f32w_plain(p, L, sms, &nchunk, s))
+                        : (gres ? launch_bwd_bf16w_gres(p, L, sms, &nchunk, s)
+                                : launch_bwd_bf16w_plain(p, L, sms, &nchunk, s));
     if (e != cudaSuccess) return e;
     return launch_dw_reduce(p.part, nchunk, p.H, dw, s);
 }

@@ -40,53 +40,67 @@ __device__ __forceinline__ uint32_t pack_fp8(float lo, float hi)
 }
 
 // ------------------------------------------------------ packed FP32 pairs --
-// Blackwell executes two FP32 operations per instruction on a 64-bit register
-// pair (add/mul/fma .rn.f32x2); each lane rounds exactly like the scalar
-// IEEE operation, so these only halve the instruction count.
+// Blackwell executes two FP32 operations per instruction on a register pair
+// (add/mul/fma .rn.f32x2, reached through the float2 builtins, which leave
+// the pairing of registers to the compiler); each lane rounds exactly like
+// the scalar IEEE operation, subnormal operands and results included (no
+// flush to zero), so these only halve the instruction count.
 
-struct F2 {
-    unsigned long long v;
-};
+using F2 = float2;
 
-__device__ __forceinline__ F2 f2(float lo, float hi)
-{
-    F2 r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(lo), "f"(hi));
-    return r;
-}
-__device__ __forceinline__ F2 f2(float a) { return f2(a, a); }
-__device__ __forceinline__ float f2_lo(F2 a)
-{
-    float lo;
-    asm("mov.b64 {%0, _}, %1;" : "=f"(lo) : "l"(a.v));
-    return lo;
-}
-__device__ __forceinline__ float f2_hi(F2 a)
-{
-    float hi;
-    asm("mov.b64 {_, %0}, %1;" : "=f"(hi) : "l"(a.v));
-    return hi;
-}
-__device__ __forceinline__ F2 f2_add(F2 a, F2 b)
-{
-    F2 r;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
-    return r;
-}
-__device__ __forceinline__ F2 f2_mul(F2 a, F2 b)
-{
-    F2 r;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
-    return r;
-}
-__device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c)
-{
-    F2 r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
-    return r;
-}
+__device__ __forceinline__ F2 f2(float lo, float hi) { return make_float2(lo, hi); }
+__device__ __forceinline__ F2 f2(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float f2_lo(F2 a) { return a.x; }
+__device__ __forceinline__ float f2_hi(F2 a) { return a.y; }
+__device__ __forceinline__ F2 f2_add(F2 a, F2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ F2 f2_mul(F2 a, F2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ F2 f2_fma(F2 a, F2 b, F2 c) { return __ffma2_rn(a, b, c); }
 // Packed BF16 pair -> FP32 pair (exact).
 __device__ __forceinline__ F2 f2_bf16(uint32_t w) { return f2(bf_lo(w), bf_hi(w)); }
+
+// ------------------------------------------------- mixed-precision BF16 --
+// Blackwell's mixed-precision FMA takes BF16 multiplicands straight from the
+// halves of a packed word (FP32 addend and result), so products of BF16
+// values need no unpacking.  A product of two BF16 values has at most 16
+// significant bits, so it is exact in FP32.
+
+// (lo(a)*lo(b), hi(a)*hi(b)) of two packed BF16 pairs, exact.
+__device__ __forceinline__ F2 mul_bf16x2(uint32_t a, uint32_t b)
+{
+    float lo, hi;
+    asm("{\n\t.reg .b16 a0, a1, b0, b1;\n\tmov.b32 {a0, a1}, %2;\n\tmov.b32 {b0, b1}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, a0, b0, %4;\n\tfma.rn.f32.bf16 %1, a1, b1, %4;\n}"
+        : "=f"(lo), "=f"(hi) : "r"(a), "r"(b), "f"(-0.f));
+    return f2(lo, hi);
+}
+
+// (lo(h) + c, hi(h) + c): the FP32 sums of the halves of a packed BF16 pair
+// and an FP32 value, one rounding each (the same bits as unpacking first).
+__device__ __forceinline__ F2 add_bf16x2(uint32_t h, float c)
+{
+    float lo, hi;
+    asm("{\n\t.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+        "add.rn.f32.bf16 %0, h0, %3;\n\tadd.rn.f32.bf16 %1, h1, %3;\n}"
+        : "=f"(lo), "=f"(hi) : "r"(h), "f"(c));
+    return f2(lo, hi);
+}
+
+// lo += lo(h), hi += hi(h) for a packed BF16 pair h (one rounding each).
+__device__ __forceinline__ void acc_bf16x2(uint32_t h, float &lo, float &hi)
+{
+    asm("{\n\t.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+        "add.rn.f32.bf16 %0, h0, %0;\n\tadd.rn.f32.bf16 %1, h1, %1;\n}"
+        : "+f"(lo), "+f"(hi) : "r"(h));
+}
+
+// lo += lo(h)^2, hi += hi(h)^2 for a packed BF16 pair h (each square exact,
+// one rounding per addition).
+__device__ __forceinline__ void sq_acc_bf16x2(uint32_t h, float &lo, float &hi)
+{
+    asm("{\n\t.reg .b16 h0, h1;\n\tmov.b32 {h0, h1}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, h0, h0, %0;\n\tfma.rn.f32.bf16 %1, h1, h1, %1;\n}"
+        : "+f"(lo), "+f"(hi) : "r"(h));
+}
 
 // ------------------------------------------------------ division by a scale --
 // v / s rounded to nearest (the IEEE quotient) for a pair v and one divisor s
@@ -98,8 +112,9 @@ __device__ __forceinline__ F2 f2_bf16(uint32_t w) { return f2(bf_lo(w), bf_hi(w)
 // reciprocal and q is within one ulp of v/s, the remainder is exact and the
 // corrected quotient is correctly rounded; the first correction brings
 // RN(v*r) (within 1.5 ulps) within one ulp.  This needs the quotient and the
-// remainder to be normal FP32 numbers (the packed instructions flush
-// subnormal results).
+// remainder to be normal FP32 numbers: a remainder below 2^-126 is rounded
+// to the subnormal grid, so dividends below 2^-96 (for |s| >= 2^-60) are
+// left to the caller, whose FP8 codes are zero there.
 __device__ __forceinline__ F2 f2_div_recip(F2 v, float s, float r)
 {
     const F2 ns = f2(-s), r2 = f2(r);
@@ -110,13 +125,13 @@ __device__ __forceinline__ F2 f2_div_recip(F2 v, float s, float r)
     return f2_fma(e, r2, q);
 }
 
-// Division of FP8 epilogue values by one scale s.  For |s| in [2^-60, 2^60]
-// the quotient is the IEEE quotient v / s whenever |v| >= 2^-96 and the
-// quotient is finite; a smaller dividend has a quotient below 2^-36, which
-// every FP8 format rounds to zero whatever its last bits, and a quotient
-// beyond the FP32 range (a dividend of 2^68 or more: a normalised value of
-// magnitude <= sqrt(H) times a weight of 2^61 or more) comes out as NaN
-// instead of an infinity.  Other scales use the IEEE division itself.
+// Division by one scale s (the 1x128 block quantiser's f32(amax / 448),
+// whose codes must equal those of the IEEE quotient bit for bit).  For |s|
+// in [2^-60, 2^60] the quotient is the IEEE quotient v / s whenever
+// |v| >= 2^-96 and the quotient is finite; a smaller dividend has a quotient
+// below 2^-36, which every FP8 format rounds to zero whatever its last bits,
+// and a quotient beyond the FP32 range comes out as NaN instead of an
+// infinity.  Other scales use the IEEE division itself.
 struct DivScale {
     float s, r;
     bool fast;
@@ -137,28 +152,19 @@ struct DivScale {
             hi = __fdiv_rn(f2_hi(v), s);
         }
     }
-    // n pairs at once, the choice between the two forms taken once.
-    template <int N>
-    __device__ __forceinline__ void div_n(const F2 (&v)[N], float (&lo)[N], float (&hi)[N]) const
-    {
-        if (fast) {
-#pragma unroll
-            for (int i = 0; i < N; ++i) {
-                const F2 q = f2_div_recip(v[i], s, r);
-                lo[i] = f2_lo(q);
-                hi[i] = f2_hi(q);
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < N; ++i) {
-                lo[i] = __fdiv_rn(f2_lo(v[i]), s);
-                hi[i] = __fdiv_rn(f2_hi(v[i]), s);
-            }
-        }
-    }
 };
 // FP32 pair -> packed BF16 pair, round to nearest even.
 __device__ __forceinline__ uint32_t bf16_f2(F2 a) { return pack_bf16(f2_lo(a), f2_hi(a)); }
+
+// Row group of a thread when a CTA holds `rpc` groups of `tpr` threads: no
+// division for one group per CTA or a power-of-two group width (every layout
+// but a few narrow ones).
+__device__ __forceinline__ int row_group(int tpr, int rpc)
+{
+    if (rpc == 1) return 0;
+    if ((tpr & (tpr - 1)) == 0) return (int)threadIdx.x >> (31 - __clz(tpr));
+    return (int)threadIdx.x / tpr;
+}
 
 // ------------------------------------------------------------ vectors ----
 // VEC BF16 elements = VEC/2 packed words.  VEC is 8 (16-byte accesses) or 2

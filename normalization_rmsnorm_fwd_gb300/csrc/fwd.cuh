@@ -92,20 +92,23 @@ __device__ __forceinline__ F2 silu_f2(F2 v)
 // L2, 2 = loaded into registers (measured per epilogue).
 constexpr int fwd_prefetch(int in, int out) { return in == IN_LAYERNORM || out == OUT_Q ? 2 : 1; }
 
-// The kernel body.
-template <int IN, bool W32, int OUT, int FP8K, int VEC, int VPT, bool SUB, bool LOOP>
+// The kernel body.  WK is the weight kind (WK_MIX: BF16 weight, no bias,
+// kept packed and multiplied by h exactly with the mixed-precision FMA;
+// WK_BF16 / WK_F32: the effective weight f32(w + bias) in FP32 registers).
+template <int IN, int WK, int OUT, int FP8K, int VEC, int VPT, bool SUB, bool LOOP>
 __device__ __forceinline__ void fwd_body(const FwdParams &p)
 {
     constexpr int NW = VEC / 2;
     constexpr bool ADA = (OUT == OUT_ADA || OUT == OUT_ADA_Q);
     constexpr bool LN = (IN == IN_LAYERNORM);
+    constexpr bool WMIX = (WK == WK_MIX) && !LN;
     // Per-warp partial sums of a multi-warp row group.  The persistent form
     // alternates two planes by row parity: the warps of a group write row
     // i+1's slots while slower warps may still read row i's, and only the
     // barrier of row i+1 orders those writes after row i's reads, so row
     // i+2 can reuse plane i's slots.  LayerNorm's two reductions per row
-    // already alternate red2_h and red_h, a barrier between every reuse.
-    __shared__ float red_h[2][32], red_l[2][32];
+    // use red2_h and then red_h[0], a barrier between every reuse.
+    __shared__ float red_h[2][32];
     __shared__ float red2_h[LN ? 32 : 1];
     // Programmatic dependent launch: wait for the preceding grid (and its
     // memory) before any global access; let the next grid be scheduled now
@@ -114,20 +117,26 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const int tpr = p.tpr;
-    const int grp = threadIdx.x / tpr;
+    const int grp = row_group(tpr, p.rpc);
     const int lane = threadIdx.x - grp * tpr;
     const int nvec = p.H / VEC;
 
     // ---------------- phase 1: loads ---------------------------------------
-    // Weights: row-independent, in registers.  LayerNorm's gamma and beta do
-    // not stay in registers through its two reductions: the persistent form
-    // keeps them in shared memory (loaded once per CTA), the one-row form
-    // loads them in its epilogue, vector by vector.
+    // Weights: row-independent, in registers (packed BF16 for WK_MIX, else
+    // the FP32 effective weight).  LayerNorm's gamma and beta do not stay in
+    // registers through its two reductions: the persistent form keeps them
+    // in shared memory (loaded once per CTA), the one-row form loads them in
+    // its epilogue, vector by vector.
     constexpr bool LN_SMEM = LN && LOOP;
     constexpr bool LN_LATE = LN && !LOOP;
-    // LN_SMEM: gamma then beta, 2H floats; for 16-byte vectors each stored as
-    // two planes (the first and the last four values of every vector), so
-    // that a warp's 16-byte reads of consecutive vectors hit distinct banks.
+    // The persistent AdaRMSNorm form (a broadcast style row) keeps 1 + scale
+    // and shift as FP32 in shared memory (converted once per CTA, the same
+    // bits as per row) and the gate chunk of its columns in registers.
+    constexpr bool ADA_SMEM = ADA && LOOP;
+    // LN_SMEM / ADA_SMEM table: gamma then beta (1 + scale then shift), 2H
+    // floats; for 16-byte vectors each stored as two planes (the first and
+    // the last four values of every vector), so that a warp's 16-byte reads
+    // of consecutive vectors hit distinct banks.
     extern __shared__ __align__(16) unsigned char fwd_dyn_smem[];
     float *const ln_gb = reinterpret_cast<float *>(fwd_dyn_smem);
     BVec<VEC> wb[VPT];
@@ -137,10 +146,20 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
         const int v = k * tpr + lane;
         if (v < nvec) {
             const int64_t c = (int64_t)v * VEC;
-            if constexpr (W32)
+            if constexpr (WK == WK_F32) {
                 ld_f32_keep<VEC>(static_cast<const float *>(p.w) + c, wf[k]);
-            else
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) wf[k][i] = __fadd_rn(wf[k][i], p.bias);
+            } else if constexpr (WK == WK_BF16) {
+                const BVec<VEC> b = ld_keep<VEC>(static_cast<const uint16_t *>(p.w) + c);
+#pragma unroll
+                for (int i = 0; i < NW; ++i) {
+                    wf[k][2 * i] = __fadd_rn(bf_lo(b.w[i]), p.bias);
+                    wf[k][2 * i + 1] = __fadd_rn(bf_hi(b.w[i]), p.bias);
+                }
+            } else {
                 wb[k] = ld_keep<VEC>(static_cast<const uint16_t *>(p.w) + c);
+            }
         } else {
 #pragma unroll
             for (int i = 0; i < NW; ++i) wb[k].w[i] = 0u;
@@ -170,7 +189,7 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
                     ra[k] = ld_stream<VEC>(p.r + t * p.ldr + c);
                 if constexpr (IN == IN_GATED)
                     ga[k] = ld_stream<VEC>(p.gate + t * p.ldgate + c);
-                if constexpr (ADA) {
+                if constexpr (ADA && !ADA_SMEM) {
                     const uint16_t *srow = p.style + t * p.lds;
                     if (p.lds == 0) {
                         sc[k] = ld_keep<VEC>(srow + c);
@@ -195,19 +214,50 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
     // Phases 2-4 of row t, whose inputs are in xa (and ra, ga, sc, sh, gt).
     // Every thread of the CTA calls it the same number of times (it may
     // contain CTA barriers).
-    // The static FP8 scale: read once (after the dependency wait at the top).
-    float scale_v = 1.f;
+    // The static FP8 scale, read once (after the dependency wait at the top)
+    // as its correctly rounded reciprocal: the epilogues multiply by it
+    // (for the plain static-scale form folded into rstd), within a few FP32
+    // ulps of the quotient v / scale, so a code can differ from the one of
+    // the exact quotient only next to a rounding midpoint.
+    float inv_scale = 1.f;
     if constexpr (OUT == OUT_Q || OUT == OUT_ADA_Q)
-        scale_v = __ldg(p.scale);
+        inv_scale = __frcp_rn(__ldg(p.scale));
     if constexpr (OUT == OUT_SILU_Q)
-        scale_v = p.scale != nullptr ? __ldg(p.scale) : 1.f;
-    const DivScale dsc(scale_v);            // IEEE division by the scale
+        inv_scale = p.scale != nullptr ? __frcp_rn(__ldg(p.scale)) : 1.f;
+    // The static-scale RMSNorm form scales rstd instead of every value.
+    constexpr bool FOLD_SCALE = OUT == OUT_Q && !LN;
+
+    // Sum over the row group of one FP32 value per thread, in plain FP32 and
+    // a fixed order: a butterfly within each warp (within the group for
+    // groups of <= 32 threads), then, across the group's warps, every warp
+    // adds the group's per-warp slots in the same butterfly.  Every thread
+    // of the group gets the same bits.  (The statistics are sums of
+    // non-negative squares, or LayerNorm's mean and squared deviations; a
+    // fixed FP32 tree keeps rstd within a few FP32 ulps.)
+    auto row_sum = [&](float v, float *rh) -> float {
+        const int width = SUB ? tpr : 32;
+        for (int o = width >> 1; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if constexpr (!SUB) {
+            const int nwarp = tpr >> 5;
+            const int warp = threadIdx.x >> 5;
+            if ((threadIdx.x & 31) == 0) rh[warp] = v;
+            __syncthreads();
+            int w = 1;
+            while (w < nwarp) w <<= 1;
+            const int i = threadIdx.x & (w - 1);
+            v = i < nwarp ? rh[grp * nwarp + i] : 0.f;
+            for (int o = w >> 1; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+        }
+        return v;
+    };
 
     auto process = [&](int64_t t, int par) {
         const bool live = t < p.T;
         // ---------------- phase 2: normalised input h, sum of squares ---------
         BVec<VEC> h[VPT];
-        F2 ss2 = f2(0.f);
+        // Four independent chains: the sum of squares (RMSNorm) or of h
+        // (LayerNorm's mean).
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
 #pragma unroll
@@ -223,15 +273,15 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
                 } else {
                     // bf16(x * gate) first (the FP32 product of two BF16 values is
                     // exact), then the BF16 residual add.
-                    const uint32_t pw = bf16_f2(f2_mul(f2_bf16(xw), f2_bf16(ga[k].w[i])));
+                    const uint32_t pw = bf16_f2(mul_bf16x2(xw, ga[k].w[i]));
                     hw = bf16_f2(f2_add(f2_bf16(ra[k].w[i]), f2_bf16(pw)));
                 }
                 h[k].w[i] = hw;
-                const F2 h2 = f2_bf16(hw);
+                const int j = (k * NW + i) & 1;
                 if constexpr (LN)
-                    ss2 = f2_add(h2, ss2);          // sum of h (the mean comes first)
+                    acc_bf16x2(hw, acc[2 * j], acc[2 * j + 1]);     // sum of h (the mean first)
                 else
-                    ss2 = f2_fma(h2, h2, ss2);      // h^2 is exact in FP32: one rounding
+                    sq_acc_bf16x2(hw, acc[2 * j], acc[2 * j + 1]);  // h^2 exact, one rounding each
             }
             if constexpr (IN != IN_PLAIN && !LN) {
                 const int v = k * tpr + lane;
@@ -241,47 +291,6 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
         }
 
         // ---------------- phase 3: row reduction -> rstd ----------------------
-        // Compensated sum over the row group of a per-thread FP32 pair: shuffles
-        // within a group of <= 32 threads; otherwise a butterfly within each warp,
-        // then across the group's warps (short latency for these short-lived CTAs).
-        auto row_sum = [&](F2 part, float *rh, float *rl) -> float {
-            float sh_, sl_;
-            two_sum(f2_lo(part), f2_hi(part), sh_, sl_);
-            if constexpr (SUB) {
-                pair_reduce_lanes(sh_, sl_, tpr);
-            } else {
-                pair_reduce_lanes(sh_, sl_, 32);
-                const int nwarp = tpr >> 5;
-                const int warp = threadIdx.x >> 5;
-                if ((threadIdx.x & 31) == 0) {
-                    rh[warp] = sh_;
-                    rl[warp] = sl_;
-                }
-                __syncthreads();
-                pair_reduce_warps(sh_, sl_, rh, rl, grp * nwarp, nwarp);
-            }
-            return __fadd_rn(sh_, sl_);
-        };
-        // The same sum in plain FP32 (a fixed butterfly, then the group's
-        // warps in a fixed tree): LayerNorm's two sums, whose accuracy needs
-        // are met without compensation.
-        auto row_sum_plain = [&](F2 part, float *rh) -> float {
-            float v = __fadd_rn(f2_lo(part), f2_hi(part));
-            const int width = SUB ? tpr : 32;
-            for (int o = width >> 1; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
-            if constexpr (!SUB) {
-                const int nwarp = tpr >> 5;
-                const int warp = threadIdx.x >> 5;
-                if ((threadIdx.x & 31) == 0) rh[warp] = v;
-                __syncthreads();
-                int w = 1;
-                while (w < nwarp) w <<= 1;
-                const int i = threadIdx.x & (w - 1);
-                v = i < nwarp ? rh[grp * nwarp + i] : 0.f;
-                for (int o = w >> 1; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
-            }
-            return v;
-        };
         // The row's FP32 values are unpacked again from the BF16 words after
         // each reduction instead of being kept (twice the registers) across
         // it: the empty asm makes the words opaque to the compiler.  Measured
@@ -297,44 +306,51 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
                     for (int i = 0; i < NW; ++i) asm volatile("" : "+r"(h[k].w[i]));
             }
         };
+        const float part = __fadd_rn(__fadd_rn(acc[0], acc[2]), __fadd_rn(acc[1], acc[3]));
         float mean = 0.f;
+        float ssum;
         if constexpr (LN) {
-            mean = __fdiv_rn(row_sum_plain(ss2, red2_h), (float)p.H);
+            mean = __fdiv_rn(row_sum(part, red2_h), (float)p.H);
             reunpack();
-            // Squared deviations of this thread's elements (none past the row).
-            const F2 nm2 = f2(-mean);
-            ss2 = f2(0.f);
+            // Squared deviations of this thread's elements (none past the row),
+            // h - mean formed from the BF16 halves directly.
+            F2 ss2 = f2(0.f);
 #pragma unroll
             for (int k = 0; k < VPT; ++k) {
                 const bool ok = live && k * tpr + lane < nvec;
 #pragma unroll
                 for (int i = 0; i < NW; ++i) {
-                    const F2 d = f2_add(f2_bf16(h[k].w[i]), nm2);
+                    const F2 d = add_bf16x2(h[k].w[i], -mean);
                     if (ok) ss2 = f2_fma(d, d, ss2);
                 }
             }
             if (p.mean != nullptr && live && lane == 0)
                 p.mean[t] = mean;
+            ssum = row_sum(__fadd_rn(f2_lo(ss2), f2_hi(ss2)), red_h[0]);
+        } else {
+            ssum = row_sum(part, red_h[par]);
         }
-        float ssum;
-        if constexpr (LN) ssum = row_sum_plain(ss2, red_h[0]);
-        else ssum = row_sum(ss2, red_h[par], red_l[par]);
         reunpack();
         const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ssum, (float)p.H), p.eps)));
         if (p.rstd != nullptr && live && lane == 0)
             p.rstd[t] = rstd;
 
         // ---------------- phase 4: epilogue -----------------------------------
-        const F2 nmean2 = f2(-mean);
-        const F2 rstd2 = f2(rstd);
-        const F2 bias2 = f2(p.bias);
+        // o = (h * w) * rstd with h * w exact (WK_MIX), or (h * rstd) * w_eff;
+        // for the static FP8 form rstd carries the reciprocal scale.
+        // The fold needs rstd / scale to be a normal FP32 number (a tiny scale
+        // and an eps-sized row can overflow it); otherwise each value is scaled.
+        const float rq = __fmul_rn(rstd, inv_scale);
+        const bool folded = FOLD_SCALE && fabsf(rq) <= 0x1.fffffep127f && fabsf(rq) >= 0x1p-126f;
+        const F2 rstd2 = f2(folded ? rq : rstd);
+        const F2 inv2 = f2(inv_scale);
 
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int v = k * tpr + lane;
             const bool ok = live && v < nvec;
             const int64_t c = (int64_t)v * VEC;
-            if constexpr (LN_SMEM) {
+            if constexpr (LN_SMEM || ADA_SMEM) {
                 if (v < nvec) {
                     if constexpr (VEC == 8) {
                         const int hp = p.H >> 1;
@@ -363,12 +379,13 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
             F2 o[NW];
 #pragma unroll
             for (int i = 0; i < NW; ++i) {
-                const F2 w2 = W32 ? f2(wf[k][2 * i], wf[k][2 * i + 1]) : f2_bf16(wb[k].w[i]);
                 if constexpr (LN)
-                    o[i] = f2_fma(f2_mul(f2_add(f2_bf16(h[k].w[i]), nmean2), rstd2), w2,
-                                  f2(bt[k][2 * i], bt[k][2 * i + 1]));
+                    o[i] = f2_fma(f2_mul(add_bf16x2(h[k].w[i], -mean), rstd2),
+                                  f2(wf[k][2 * i], wf[k][2 * i + 1]), f2(bt[k][2 * i], bt[k][2 * i + 1]));
+                else if constexpr (WMIX)
+                    o[i] = f2_mul(mul_bf16x2(h[k].w[i], wb[k].w[i]), rstd2);
                 else
-                    o[i] = f2_mul(f2_mul(f2_bf16(h[k].w[i]), rstd2), f2_add(w2, bias2));
+                    o[i] = f2_mul(f2_mul(f2_bf16(h[k].w[i]), rstd2), f2(wf[k][2 * i], wf[k][2 * i + 1]));
             }
 
             if constexpr (OUT == OUT_Y) {
@@ -378,10 +395,11 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
                 if (ok) st_stream<VEC>(p.y + t * p.ldy + c, yv);
             } else if constexpr (OUT == OUT_Q) {
                 uint32_t cq[NW];
-                float a[NW], b[NW];
-                dsc.div_n(o, a, b);
 #pragma unroll
-                for (int i = 0; i < NW; ++i) cq[i] = pack_fp8<FP8K>(a[i], b[i]);
+                for (int i = 0; i < NW; ++i) {
+                    const F2 v = folded ? o[i] : f2_mul(o[i], inv2);
+                    cq[i] = pack_fp8<FP8K>(f2_lo(v), f2_hi(v));
+                }
                 if (ok) st_fp8<VEC>(p.q + t * p.ldq + c, cq);
             } else if constexpr (OUT == OUT_BLOCK) {
                 // normed = bf16(o); amax over the 128-column block held by 16
@@ -431,8 +449,8 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
                 } else {
 #pragma unroll
                     for (int i = 0; i < NW; ++i) {
-                        const F2 y2 = silu_f2(o[i]);
-                        cq[i] = pack_fp8<0>(__fdiv_rn(f2_lo(y2), scale_v), __fdiv_rn(f2_hi(y2), scale_v));
+                        const F2 y2 = f2_mul(silu_f2(o[i]), inv2);
+                        cq[i] = pack_fp8<0>(f2_lo(y2), f2_hi(y2));
                     }
                 }
                 if (ok) st_fp8<VEC>(p.q + t * p.ldq + c, cq);
@@ -440,8 +458,12 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
                 const F2 one2 = f2(1.f);
                 F2 ov[NW];
 #pragma unroll
-                for (int i = 0; i < NW; ++i)
-                    ov[i] = f2_fma(o[i], f2_add(one2, f2_bf16(sc[k].w[i])), f2_bf16(sh[k].w[i]));
+                for (int i = 0; i < NW; ++i) {
+                    if constexpr (ADA_SMEM)
+                        ov[i] = f2_fma(o[i], f2(wf[k][2 * i], wf[k][2 * i + 1]), f2(bt[k][2 * i], bt[k][2 * i + 1]));
+                    else
+                        ov[i] = f2_fma(o[i], f2_add(one2, f2_bf16(sc[k].w[i])), f2_bf16(sh[k].w[i]));
+                }
                 if constexpr (OUT == OUT_ADA) {
                     BVec<VEC> out;
 #pragma unroll
@@ -449,10 +471,11 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
                     if (ok) st_stream<VEC>(p.y + t * p.ldy + c, out);
                 } else {
                     uint32_t cq[NW];
-                    float a[NW], b[NW];
-                    dsc.div_n(ov, a, b);
 #pragma unroll
-                    for (int i = 0; i < NW; ++i) cq[i] = pack_fp8<0>(a[i], b[i]);
+                    for (int i = 0; i < NW; ++i) {
+                        const F2 v = f2_mul(ov[i], inv2);
+                        cq[i] = pack_fp8<0>(f2_lo(v), f2_hi(v));
+                    }
                     if (ok) st_fp8<VEC>(p.q + t * p.ldq + c, cq);
                 }
                 if (ok) st_stream<VEC>(p.gate_out + t * p.ldgo + c, gt[k]);
@@ -465,7 +488,7 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
         load_row(t, xa, true);
         process(t, 0);
     } else {
-        static_assert(IN == IN_PLAIN || LN, "the persistent form streams one input");
+        static_assert(IN == IN_PLAIN || LN || ADA, "no persistent form for this input");
         load_weights();
         const int64_t stride = (int64_t)gridDim.x * p.rpc;
         const int64_t b0 = (int64_t)blockIdx.x * p.rpc;
@@ -492,25 +515,74 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
             }
             __syncthreads();
         }
+        if constexpr (ADA_SMEM) {
+            // 1 + scale and shift of the broadcast style row into shared
+            // memory (the whole CTA striding over the vectors); the gate
+            // chunk of this thread's columns into registers.
+            for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+                const int64_t c = (int64_t)v * VEC;
+                const BVec<VEC> a = ld_keep<VEC>(p.style + c);
+                const BVec<VEC> b = ld_keep<VEC>(p.style + p.H + c);
+                float g[VEC], f[VEC];
+#pragma unroll
+                for (int i = 0; i < NW; ++i) {
+                    const F2 s1 = f2_add(f2(1.f), f2_bf16(a.w[i]));
+                    const F2 sf = f2_bf16(b.w[i]);
+                    g[2 * i] = f2_lo(s1); g[2 * i + 1] = f2_hi(s1);
+                    f[2 * i] = f2_lo(sf); f[2 * i + 1] = f2_hi(sf);
+                }
+                if constexpr (VEC == 8) {
+                    const int hp = p.H >> 1;
+                    st_smem_f32x4(ln_gb + v * 4, g);
+                    st_smem_f32x4(ln_gb + hp + v * 4, g + 4);
+                    st_smem_f32x4(ln_gb + p.H + v * 4, f);
+                    st_smem_f32x4(ln_gb + p.H + hp + v * 4, f + 4);
+                } else {
+                    *reinterpret_cast<float2 *>(ln_gb + v * 2) = make_float2(g[0], g[1]);
+                    *reinterpret_cast<float2 *>(ln_gb + p.H + v * 2) = make_float2(f[0], f[1]);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int v = k * tpr + lane;
+                if (v < nvec) {
+                    gt[k] = ld_keep<VEC>(p.style + 2 * p.H + (int64_t)v * VEC);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < NW; ++i) gt[k].w[i] = 0u;
+                }
+            }
+            __syncthreads();
+        }
         // The next row is loaded into registers before this row is processed
         // (PF == 2), or only prefetched into L2 then and loaded afterwards
-        // (PF == 1: no registers held across the row).
+        // (PF == 1: no registers held across the row); the row after it is
+        // prefetched into L2 as well, so two rows per group are in flight.
+        auto prefetch_l2 = [&](int64_t t) {
+            if (t < p.T) {
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    const int v = k * tpr + lane;
+                    if (v < nvec) {
+                        const int64_t c = (int64_t)v * VEC;
+                        asm volatile("prefetch.global.L2 [%0];" :: "l"(p.x + t * p.ldx + c));
+                        if constexpr (IN == IN_GATED) {
+                            asm volatile("prefetch.global.L2 [%0];" :: "l"(p.r + t * p.ldr + c));
+                            asm volatile("prefetch.global.L2 [%0];" :: "l"(p.gate + t * p.ldgate + c));
+                        }
+                    }
+                }
+            }
+        };
+        if constexpr (PF == 1) prefetch_l2(b0 + stride + grp);
         int par = 0;
         for (int64_t base = b0; base < p.T; base += stride, par ^= 1) {
             BVec<VEC> xn[VPT];
             const bool more = base + stride < p.T;   // the same for the whole CTA
             const int64_t tn = base + stride + grp;
-            if (more) {
-                if constexpr (PF == 2) {
-                    load_row(tn, xn, false);
-                } else if (tn < p.T) {
-#pragma unroll
-                    for (int k = 0; k < VPT; ++k) {
-                        const int v = k * tpr + lane;
-                        if (v < nvec)
-                            asm volatile("prefetch.global.L2 [%0];" :: "l"(p.x + tn * p.ldx + (int64_t)v * VEC));
-                    }
-                }
+            prefetch_l2(tn + stride);
+            if constexpr (PF == 2) {
+                if (more) load_row(tn, xn, false);
             }
             process(base + grp, par);
             if (more) {
@@ -527,19 +599,19 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
 
 // No minimum CTA count in the launch bounds: an explicit one (even 1) lets
 // the compiler take far more registers for these kernels.
-template <int IN, bool W32, int OUT, int FP8K, int VEC, int VPT, bool SUB, bool LOOP>
+template <int IN, int WK, int OUT, int FP8K, int VEC, int VPT, bool SUB, bool LOOP>
 __global__ void __launch_bounds__(kFwdMaxThreads) k_rmsnorm_fwd(const FwdParams p)
 {
-    fwd_body<IN, W32, OUT, FP8K, VEC, VPT, SUB, LOOP>(p);
+    fwd_body<IN, WK, OUT, FP8K, VEC, VPT, SUB, LOOP>(p);
 }
 
 // Host-side launch of one kernel.  The persistent form runs on at most
 // (resident CTAs per SM) x (SMs) CTAs; the residency for a block size and
 // shared-memory size is computed once and remembered.
-template <int IN, bool W32, int OUT, int FP8K, int VEC, int VPT, bool SUB, bool LOOP>
+template <int IN, int WK, int OUT, int FP8K, int VEC, int VPT, bool SUB, bool LOOP>
 cudaError_t launch_fwd_kernel(const FwdParams &p, size_t smem, cudaStream_t s)
 {
-    auto kern = k_rmsnorm_fwd<IN, W32, OUT, FP8K, VEC, VPT, SUB, LOOP>;
+    auto kern = k_rmsnorm_fwd<IN, WK, OUT, FP8K, VEC, VPT, SUB, LOOP>;
     const int threads = p.tpr * p.rpc;
     int64_t blocks = (p.T + p.rpc - 1) / p.rpc;
     if (smem > 0) {
@@ -575,49 +647,57 @@ cudaError_t launch_fwd_kernel(const FwdParams &p, size_t smem, cudaStream_t s)
 constexpr size_t kLnSmemMax = 64 * 1024;
 
 // Launch of one instantiation.  Measured: the persistent form pays off for
-// the plain row with the y and static FP8 epilogues and for LayerNorm with
-// gamma and beta in shared memory; SiLU (bound by its arithmetic) runs
-// faster in the one-row form.
-template <int IN, bool W32, int OUT, int FP8K, int VEC, int VPT, bool SUB>
+// the plain row with the y and static FP8 epilogues, for LayerNorm with
+// gamma and beta in shared memory and for AdaRMSNorm with a broadcast style
+// row in shared memory; SiLU (bound by its arithmetic) runs faster in the
+// one-row form.
+template <int IN, int WK, int OUT, int FP8K, int VEC, int VPT, bool SUB>
 cudaError_t launch_fwd_inst(const FwdParams &p, cudaStream_t s)
 {
     if constexpr (IN == IN_LAYERNORM) {
         const size_t table = (size_t)2 * p.H * sizeof(float);
         if (table <= kLnSmemMax)
-            return launch_fwd_kernel<IN, W32, OUT, FP8K, VEC, VPT, SUB, true>(p, table, s);
-        return launch_fwd_kernel<IN, W32, OUT, FP8K, VEC, VPT, SUB, false>(p, 0, s);
+            return launch_fwd_kernel<IN, WK, OUT, FP8K, VEC, VPT, SUB, true>(p, table, s);
+        return launch_fwd_kernel<IN, WK, OUT, FP8K, VEC, VPT, SUB, false>(p, 0, s);
+    } else if constexpr (OUT == OUT_ADA || OUT == OUT_ADA_Q) {
+        // A broadcast style row (lds == 0): the persistent form with the
+        // style's 1 + scale and shift in shared memory (2H floats).
+        if (p.lds == 0)
+            return launch_fwd_kernel<IN, WK, OUT, FP8K, VEC, VPT, SUB, true>(
+                p, (size_t)2 * p.H * sizeof(float), s);
+        return launch_fwd_kernel<IN, WK, OUT, FP8K, VEC, VPT, SUB, false>(p, 0, s);
     } else {
         constexpr bool LOOP = IN == IN_PLAIN && (OUT == OUT_Y || OUT == OUT_Q);
-        return launch_fwd_kernel<IN, W32, OUT, FP8K, VEC, VPT, SUB, LOOP>(p, 0, s);
+        return launch_fwd_kernel<IN, WK, OUT, FP8K, VEC, VPT, SUB, LOOP>(p, 0, s);
     }
 }
 
 // Dispatch over the row layouts the host chooser can return: SUB groups with
 // VPT 1|2; multi-warp groups with VPT 2|4 (16-byte vectors) or 2|4|8|16
 // (4-byte vectors), i.e. at most 32 elements per thread.
-template <int IN, bool W32, int OUT, int FP8K, int VEC>
+template <int IN, int WK, int OUT, int FP8K, int VEC>
 cudaError_t launch_fwd_vec(const FwdParams &p, int vpt, bool sub, cudaStream_t s)
 {
     if (sub) {
-        if (vpt == 1) return launch_fwd_inst<IN, W32, OUT, FP8K, VEC, 1, true>(p, s);
-        if (vpt == 2) return launch_fwd_inst<IN, W32, OUT, FP8K, VEC, 2, true>(p, s);
+        if (vpt == 1) return launch_fwd_inst<IN, WK, OUT, FP8K, VEC, 1, true>(p, s);
+        if (vpt == 2) return launch_fwd_inst<IN, WK, OUT, FP8K, VEC, 2, true>(p, s);
     } else {
-        if (vpt == 2) return launch_fwd_inst<IN, W32, OUT, FP8K, VEC, 2, false>(p, s);
-        if (vpt == 4) return launch_fwd_inst<IN, W32, OUT, FP8K, VEC, 4, false>(p, s);
+        if (vpt == 2) return launch_fwd_inst<IN, WK, OUT, FP8K, VEC, 2, false>(p, s);
+        if (vpt == 4) return launch_fwd_inst<IN, WK, OUT, FP8K, VEC, 4, false>(p, s);
         if constexpr (VEC == 2) {
-            if (vpt == 8) return launch_fwd_inst<IN, W32, OUT, FP8K, VEC, 8, false>(p, s);
-            if (vpt == 16) return launch_fwd_inst<IN, W32, OUT, FP8K, VEC, 16, false>(p, s);
+            if (vpt == 8) return launch_fwd_inst<IN, WK, OUT, FP8K, VEC, 8, false>(p, s);
+            if (vpt == 16) return launch_fwd_inst<IN, WK, OUT, FP8K, VEC, 16, false>(p, s);
         }
     }
     return cudaErrorInvalidConfiguration;
 }
 
-template <int IN, bool W32, int OUT, int FP8K>
+template <int IN, int WK, int OUT, int FP8K>
 cudaError_t launch_fwd(const FwdParams &p, int vec, int vpt, bool sub, cudaStream_t s)
 {
-    if (vec == 8) return launch_fwd_vec<IN, W32, OUT, FP8K, 8>(p, vpt, sub, s);
+    if (vec == 8) return launch_fwd_vec<IN, WK, OUT, FP8K, 8>(p, vpt, sub, s);
     if constexpr (OUT != OUT_BLOCK)
-        if (vec == 2) return launch_fwd_vec<IN, W32, OUT, FP8K, 2>(p, vpt, sub, s);
+        if (vec == 2) return launch_fwd_vec<IN, WK, OUT, FP8K, 2>(p, vpt, sub, s);
     return cudaErrorInvalidConfiguration;
 }
 

@@ -4,16 +4,18 @@
 
 namespace crmsn {
 
-template <int IN, bool W32>
-static cudaError_t go(const FwdParams &p, const Layout &L, cudaStream_t s)
+template <int IN>
+static cudaError_t go(const FwdParams &p, int wk, const Layout &L, cudaStream_t s)
 {
-    return launch_fwd<IN, W32, OUT_Y, 0>(p, L.vec, L.vpt, L.sub, s);
+    if (wk == WK_MIX) return launch_fwd<IN, WK_MIX, OUT_Y, 0>(p, L.vec, L.vpt, L.sub, s);
+    if (wk == WK_BF16) return launch_fwd<IN, WK_BF16, OUT_Y, 0>(p, L.vec, L.vpt, L.sub, s);
+    return launch_fwd<IN, WK_F32, OUT_Y, 0>(p, L.vec, L.vpt, L.sub, s);
 }
 
-cudaError_t launch_fwd_y(const FwdParams &p, int in, bool w32, const Layout &L, cudaStream_t s)
+cudaError_t launch_fwd_y(const FwdParams &p, int in, int wk, const Layout &L, cudaStream_t s)
 {
-    if (in == IN_PLAIN) return w32 ? go<IN_PLAIN, true>(p, L, s) : go<IN_PLAIN, false>(p, L, s);
-    if (in == IN_RESIDUAL) return w32 ? go<IN_RESIDUAL, true>(p, L, s) : go<IN_RESIDUAL, false>(p, L, s);
+    if (in == IN_PLAIN) return go<IN_PLAIN>(p, wk, L, s);
+    if (in == IN_RESIDUAL) return go<IN_RESIDUAL>(p, wk, L, s);
     return cudaErrorInvalidValue;
 }
 

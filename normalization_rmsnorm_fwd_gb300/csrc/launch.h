@@ -15,8 +15,18 @@ namespace crmsn {
 // backward kernel.
 constexpr int kFwdMaxThreads = 512;
 constexpr int kBwdMaxThreads = 512;
-// The backward workspace holds at most this many partial rows per SM.
+// Backward CTAs per SM: at most kBwdMaxCtasPerSm, and at most as many as
+// the SM's 228 KB of shared memory can hold at the smallest ring a CTA uses
+// (two stages of g and x and the FP32 weight table: 12 bytes per column), so
+// the workspace -- one FP32 partial row per CTA -- stays below 12 MB for
+// every H on a 152-SM GB300.  (Measured at H = 4096: three or four CTAs per
+// SM of a narrower layout were slower than two of 256 threads.)
 constexpr int kBwdMaxCtasPerSm = 2;
+inline int bwd_max_ctas_per_sm(int64_t H)
+{
+    const int64_t n = (int64_t)(228 * 1024) / (12 * (H > 0 ? H : 1));
+    return n < 1 ? 1 : (n > kBwdMaxCtasPerSm ? kBwdMaxCtasPerSm : (int)n);
+}
 // Multi-warp row groups of the backward: at most this many per CTA (a group
 // has at least 96 threads and a CTA at most 256 threads' worth of groups)
 // and at most this many warps each.
@@ -24,6 +34,11 @@ constexpr int kBwdMaxGroups = 4;
 constexpr int kBwdMaxGroupWarps = kBwdMaxThreads / 32;
 
 enum InKind { IN_PLAIN = 0, IN_RESIDUAL = 1, IN_GATED = 2, IN_LAYERNORM = 3 };
+// How the forward holds the weight: WK_MIX, a BF16 weight with no bias, kept
+// as packed BF16 and multiplied by h exactly (mixed-precision FMA); WK_BF16
+// and WK_F32, the effective weight f32(w + bias) of a BF16 or FP32 weight in
+// FP32 registers.
+enum WeightKind { WK_MIX = 0, WK_BF16 = 1, WK_F32 = 2 };
 enum OutKind {
     OUT_Y = 0,         // y = bf16(o)
     OUT_Q = 1,         // q = fp8(o / scale)
@@ -140,13 +155,13 @@ cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block, size_t sm
     return e;
 }
 
-cudaError_t launch_fwd_y(const FwdParams &p, int in, bool w32, const Layout &L, cudaStream_t s);
-cudaError_t launch_fwd_q(const FwdParams &p, int in, bool w32, int fp8k, const Layout &L, cudaStream_t s);
+cudaError_t launch_fwd_y(const FwdParams &p, int in, int wk, const Layout &L, cudaStream_t s);
+cudaError_t launch_fwd_q(const FwdParams &p, int in, int wk, int fp8k, const Layout &L, cudaStream_t s);
 cudaError_t launch_fwd_block(const FwdParams &p, const Layout &L, cudaStream_t s);
 cudaError_t launch_fwd_ada(const FwdParams &p, bool gated_fp8, const Layout &L, cudaStream_t s);
 // RMSNorm + SiLU (BF16, or E4M3 when fp8) and LayerNorm (BF16 when
 // fp8k < 0, else FP8 of that kind), fwd_silu_ln.cu.
-cudaError_t launch_fwd_silu(const FwdParams &p, bool w32, bool fp8, const Layout &L, cudaStream_t s);
+cudaError_t launch_fwd_silu(const FwdParams &p, int wk, bool fp8, const Layout &L, cudaStream_t s);
 cudaError_t launch_fwd_layernorm(const FwdParams &p, int fp8k, const Layout &L, cudaStream_t s);
 
 // Backward (bwd.cu).
@@ -155,11 +170,12 @@ cudaError_t launch_fwd_layernorm(const FwdParams &p, int fp8k, const Layout &L, 
 // partial-dw kernel and then the fixed-order dw reduction (bwd_reduce.cu).
 cudaError_t launch_bwd(BwdParams p, bool w32, bool gres, const Layout &L, int sms, float *dw,
                        cudaStream_t s);
-// The dx / partial-dw kernel alone, per weight type (bwd_bf16w.cu,
-// bwd_f32w.cu); *nchunk receives the chunk count it used.
-cudaError_t launch_bwd_bf16w(const BwdParams &p, bool gres, const Layout &L, int sms, int *nchunk,
-                             cudaStream_t s);
-cudaError_t launch_bwd_f32w(const BwdParams &p, bool gres, const Layout &L, int sms, int *nchunk,
-                            cudaStream_t s);
+// The dx / partial-dw kernel alone, per weight type and g_residual
+// (bwd_bf16w.cu, bwd_bf16w_gres.cu, bwd_f32w.cu, bwd_f32w_gres.cu, compiled
+// in parallel); *nchunk receives the chunk count it used.
+cudaError_t launch_bwd_bf16w_plain(const BwdParams &p, const Layout &L, int sms, int *nchunk, cudaStream_t s);
+cudaError_t launch_bwd_bf16w_gres(const BwdParams &p, const Layout &L, int sms, int *nchunk, cudaStream_t s);
+cudaError_t launch_bwd_f32w_plain(const BwdParams &p, const Layout &L, int sms, int *nchunk, cudaStream_t s);
+cudaError_t launch_bwd_f32w_gres(const BwdParams &p, const Layout &L, int sms, int *nchunk, cudaStream_t s);
 
 }  // namespace crmsn

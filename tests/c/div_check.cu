@@ -1,4 +1,4 @@
-// Bitwise check of the FP8 epilogues' division by a scale (DivScale, five
+// Bitwise check of the block quantiser's division by a scale (DivScale, five
 // packed FMA-type instructions from the reciprocal) against CUDA's IEEE
 // division __fdiv_rn, on pseudo-random dividends and divisors over wide
 // exponent ranges plus the library's own divisors (0.04, 1, amax / 448).

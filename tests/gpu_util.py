@@ -7,7 +7,8 @@ Tolerances (the pages' accuracy contract as restated for this library):
   the exact value, i.e. either neighbour of the exact value.  Where the value
   is a difference of larger FP32 terms (dx, Ada's shift) an FP32 evaluation
   cannot be closer than the rounding of those terms, so 2^-20 * (|term1| +
-  |term2|) is added (a few FP32 ulps of the terms).
+  |term2|) is added (a few FP32 ulps of the terms); for dx also the FP32
+  rounding of m = mean(g*w*x), 2^-18 * |x| * rstd^3 * mean|g*w*x|.
 * h_new, residual updates, gate_out: bit-exact.
 * FP8 codes: equal, except one code step where the exact pre-quantisation
   value lies within a relative 2^-18 of a rounding midpoint (the FP32 value
@@ -98,11 +99,20 @@ def check_dw(got, ref, ref_abs, what="dw"):
 
 
 def dx_allowance(g_bits, x_bits, w_eff, rstd, m):
-    """2^-20 * (|rstd*g*w| + |x*rstd^3*m|) per element."""
+    """Per element: 2^-20 * (|rstd*g*w| + |x*rstd^3*m|), the FP32 evaluation
+    of dx's two terms, plus 2^-18 * |x| * rstd^3 * mean_j |g_j w_j x_j|, the
+    rounding of m itself.  m is an FP32 sum of H products (the statistics are
+    FP32), whose error is bounded by a few tens of FP32 ulps of the sum of the
+    products' magnitudes (each thread adds its at most 32 products in turn,
+    then a tree of depth <= 9 adds the threads), not of |m|: where the
+    row's products cancel, that is many times |m|."""
     g = numfmt.decode_bf16(g_bits)
     x = numfmt.decode_bf16(x_bits)
     r = np.asarray(rstd, np.float64)[:, None]
-    return 2.0 ** -20 * (np.abs(r * g * w_eff[None, :]) + np.abs(x * r ** 3 * np.asarray(m)[:, None]))
+    w = np.asarray(w_eff, np.float64)[None, :]
+    mabs = np.abs(g * w * x).mean(axis=1, keepdims=True)
+    return (2.0 ** -20 * (np.abs(r * g * w) + np.abs(x * r ** 3 * np.asarray(m)[:, None]))
+            + 2.0 ** -18 * np.abs(x) * r ** 3 * mabs)
 
 
 def row_blocks(T: int, H: int, budget: int = 1 << 20) -> list:

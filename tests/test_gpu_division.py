@@ -1,5 +1,6 @@
-"""The FP8 epilogues divide by the scale with five FMA-type instructions from
-its reciprocal (Markstein's corrections) instead of CUDA's IEEE division; this
+"""The 1x128 block quantiser divides by each block's scale with five FMA-type
+instructions from its reciprocal (Markstein's corrections) instead of CUDA's
+IEEE division, and its codes must match the IEEE quotient's bit for bit; this
 test builds tests/c/div_check.cu with nvcc and checks on about 67 million
 quotients (dividends and divisors over the whole normal range) that the two
 agree bit for bit within the stated domain and that tiny dividends give

@@ -9,7 +9,8 @@ inputs: both run the same kernels with the same chunk table.  Before each
 call the scratch is filled with NaN partial rows by a wider call whose
 gradient is NaN, so a partial row read before it was written would show.
 The first problem is also checked against the oracle on every row.  A
-problem needing more than the built-in scratch must be refused.  This file
+width whose workspace exceeds the built-in scratch must be refused without
+a launch (no width does on a 152-SM GB300).  This file
 sorts last so that a run stopping at its first failure has already run
 every other test.
 """
@@ -88,18 +89,28 @@ def test_noalloc_backward_matches_rmsnorm_bwd(orc):
             gu.check_dw(dw.cpu().numpy(), ref["dw"], ref["dw_abs"], what="dw vs oracle")
 
 
-def test_noalloc_refuses_problems_beyond_its_scratch():
+def test_noalloc_scratch_limit_is_the_workspace_size():
+    """Every width either runs (its workspace fits the 16 MiB scratch) or is
+    refused with CRMSN_ERR_SCRATCH_LIMIT and no launch, exactly as
+    rmsnorm_bwd_workspace_bytes says (on a 152-SM GB300 every width fits;
+    GPUs with many more SMs need larger workspaces)."""
     L = _abi.load()
     torch.cuda.set_device(0)
-    H = 16384
-    need = L.rmsnorm_bwd_workspace_bytes(4096, H, 0, 0)
-    assert need > 16 << 20
-    t = torch.zeros((4096, H), dtype=torch.bfloat16, device="cuda")
-    w = torch.ones(H, dtype=torch.bfloat16, device="cuda")
-    rstd = torch.ones(4096, device="cuda")
-    dw = torch.empty(H, device="cuda")
-    dx = torch.empty_like(t)
-    st = L.rmsnorm_bwd_noalloc(t.data_ptr(), H, t.data_ptr(), H, w.data_ptr(), 0, 0.0, rstd.data_ptr(),
-                               None, 0, 4096, H, dx.data_ptr(), H, dw.data_ptr(),
-                               torch.cuda.current_stream().cuda_stream)
-    assert _abi.STATUS[st] == "CRMSN_ERR_SCRATCH_LIMIT"
+    st = torch.cuda.current_stream().cuda_stream
+    T = 4
+    for H in (128, 4096, 8192, 9728, 12288, 16384):
+        need = L.rmsnorm_bwd_workspace_bytes(T, H, 0, 0)
+        t = torch.ones((T, H), dtype=torch.bfloat16, device="cuda")
+        w = torch.ones(H, dtype=torch.bfloat16, device="cuda")
+        rstd = torch.ones(T, device="cuda")
+        dw = torch.full((H,), float("nan"), device="cuda")
+        dx = torch.empty_like(t)
+        s = L.rmsnorm_bwd_noalloc(t.data_ptr(), H, t.data_ptr(), H, w.data_ptr(), 0, 0.0,
+                                  rstd.data_ptr(), None, 0, T, H, dx.data_ptr(), H, dw.data_ptr(), st)
+        torch.cuda.synchronize()
+        if need > 16 << 20:
+            assert _abi.STATUS[s] == "CRMSN_ERR_SCRATCH_LIMIT", (H, need)
+            assert torch.isnan(dw).all(), "a refused call launched"
+        else:
+            assert s == 0, (H, _abi.STATUS[s])
+            assert torch.equal(dw, torch.full_like(dw, float(T))), H   # g = x = rstd = 1
