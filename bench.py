@@ -221,10 +221,12 @@ def other_kernels(dev, peak, only=None):
     """Each hot-path kernel at its own workload, launched back to back over
     rotating input/output sets whose total is at least 2x the L2 size (at
     most 64 sets: the smallest problems stay L2-resident and are reported as
-    latency), so that no launch of a large problem finds its inputs in L2;
-    average device time per launch from one pair of CUDA events around the
-    whole loop on the launching stream.  `only`: a substring; rows whose
-    name does not contain it are skipped."""
+    latency), so that no launch of a large problem finds its inputs in L2.
+    Device time per launch: the loop of launches captured into a CUDA graph
+    and replayed, one pair of CUDA events around the replays on the
+    replaying stream (so the host's per-call cost does not hide small
+    kernels); the eager loop's time per Python call is kept as us_eager.
+    `only`: a substring; rows whose name does not contain it are skipped."""
     import torch
 
     import normalization_rmsnorm_fwd_gb300 as crm
@@ -242,19 +244,44 @@ def other_kernels(dev, peak, only=None):
         for f in sets:
             f()
         torch.cuda.synchronize()
-        st = torch.cuda.current_stream()
         n = max(launches, 2 * len(sets))
+        # Eager: one Python call per launch (for small problems the host's
+        # per-call cost, several microseconds, can exceed the kernel's).
+        st = torch.cuda.current_stream()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(st)
         for i in range(n):
             sets[i % len(sets)]()
         b.record(st)
         torch.cuda.synchronize()
-        us = a.elapsed_time(b) / n * 1e3
+        us_eager = a.elapsed_time(b) / n * 1e3
+        # Device time per launch: the same n launches captured into a CUDA
+        # graph and replayed (programmatic dependent launch kept), events
+        # around the replays on the replaying stream.
+        graph = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream()
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(graph, stream=cap):
+                for i in range(n):
+                    sets[i % len(sets)]()
+        torch.cuda.synchronize()
+        graph.replay()
+        torch.cuda.synchronize()
+        reps = 3
+        rs = torch.cuda.current_stream()
+        a.record(rs)
+        for _ in range(reps):
+            graph.replay()
+        b.record(rs)
+        torch.cuda.synchronize()
+        us = a.elapsed_time(b) / (reps * n) * 1e3
         gbs = nbytes / us / 1e3
         row = {"kernel": name, "bytes": nbytes, "us": round(us, 2), "gbs": round(gbs, 1),
-               "frac": round(gbs / peak, 4), "rotating_sets": len(sets),
+               "frac": round(gbs / peak, 4), "us_eager": round(us_eager, 2),
+               "timing": "CUDA graph of back-to-back launches", "rotating_sets": len(sets),
                "l2_resident": len(sets) * nbytes < 2 * l2}
+        del graph
         out.append(row)
         del sets
         torch.cuda.empty_cache()

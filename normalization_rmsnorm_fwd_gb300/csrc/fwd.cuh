@@ -251,10 +251,27 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
         return v;
     };
 
-    auto process = [&](int64_t t, int par) {
+    // The two halves of row_sum for a multi-warp group, with the CTA barrier
+    // between them left to the caller (the pipelined persistent loop).
+    auto publish = [&](float v, float *rh) {
+        for (int o = 16; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if ((threadIdx.x & 31) == 0) rh[threadIdx.x >> 5] = v;
+    };
+    auto gather = [&](const float *rh) -> float {
+        const int nwarp = tpr >> 5;
+        int w = 1;
+        while (w < nwarp) w <<= 1;
+        const int i = threadIdx.x & (w - 1);
+        float v = i < nwarp ? rh[grp * nwarp + i] : 0.f;
+        for (int o = w >> 1; o > 0; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+        return v;
+    };
+
+    // Phase 2 of row t from the loaded words: the normalised input h into
+    // hh (h_new stored on the residual routes) and this thread's partial sum
+    // (of h^2, or of h for LayerNorm).
+    auto phase_h = [&](int64_t t, BVec<VEC> (&h)[VPT]) -> float {
         const bool live = t < p.T;
-        // ---------------- phase 2: normalised input h, sum of squares ---------
-        BVec<VEC> h[VPT];
         // Four independent chains: the sum of squares (RMSNorm) or of h
         // (LayerNorm's mean).
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -289,7 +306,31 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
                     st_stream<VEC>(p.hn + t * p.ldh + (int64_t)v * VEC, h[k]);
             }
         }
+        return __fadd_rn(__fadd_rn(acc[0], acc[2]), __fadd_rn(acc[1], acc[3]));
+    };
 
+    // LayerNorm: this thread's sum of squared deviations from the mean (none
+    // past the row), h - mean formed from the BF16 halves directly.
+    auto dev_part = [&](int64_t t, const BVec<VEC> (&h)[VPT], float mean) -> float {
+        const bool live = t < p.T;
+        F2 ss2 = f2(0.f);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const bool ok = live && k * tpr + lane < nvec;
+#pragma unroll
+            for (int i = 0; i < NW; ++i) {
+                const F2 d = add_bf16x2(h[k].w[i], -mean);
+                if (ok) ss2 = f2_fma(d, d, ss2);
+            }
+        }
+        return __fadd_rn(f2_lo(ss2), f2_hi(ss2));
+    };
+
+    // Phases 3-4 of row t from h and its partial sum: the row reduction, rstd,
+    // the epilogue.  With `reduced` (RMSNorm only) the pipelined loop has
+    // reduced the row already and `part` is the total.
+    auto finish = [&](int64_t t, BVec<VEC> (&h)[VPT], float part, int par, bool reduced) {
+        const bool live = t < p.T;
         // ---------------- phase 3: row reduction -> rstd ----------------------
         // The row's FP32 values are unpacked again from the BF16 words after
         // each reduction instead of being kept (twice the registers) across
@@ -306,29 +347,16 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
                     for (int i = 0; i < NW; ++i) asm volatile("" : "+r"(h[k].w[i]));
             }
         };
-        const float part = __fadd_rn(__fadd_rn(acc[0], acc[2]), __fadd_rn(acc[1], acc[3]));
         float mean = 0.f;
         float ssum;
         if constexpr (LN) {
             mean = __fdiv_rn(row_sum(part, red2_h), (float)p.H);
             reunpack();
-            // Squared deviations of this thread's elements (none past the row),
-            // h - mean formed from the BF16 halves directly.
-            F2 ss2 = f2(0.f);
-#pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const bool ok = live && k * tpr + lane < nvec;
-#pragma unroll
-                for (int i = 0; i < NW; ++i) {
-                    const F2 d = add_bf16x2(h[k].w[i], -mean);
-                    if (ok) ss2 = f2_fma(d, d, ss2);
-                }
-            }
+            ssum = row_sum(dev_part(t, h, mean), red_h[0]);
             if (p.mean != nullptr && live && lane == 0)
                 p.mean[t] = mean;
-            ssum = row_sum(__fadd_rn(f2_lo(ss2), f2_hi(ss2)), red_h[0]);
         } else {
-            ssum = row_sum(part, red_h[par]);
+            ssum = reduced ? part : row_sum(part, red_h[par]);
         }
         reunpack();
         const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ssum, (float)p.H), p.eps)));
@@ -483,6 +511,12 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
         }
     };
 
+    auto process = [&](int64_t t, int par) {
+        BVec<VEC> h[VPT];
+        const float part = phase_h(t, h);
+        finish(t, h, part, par, false);
+    };
+
     if constexpr (!LOOP) {
         const int64_t t = (int64_t)blockIdx.x * p.rpc + grp;
         load_row(t, xa, true);
@@ -556,8 +590,7 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
         }
         // The next row is loaded into registers before this row is processed
         // (PF == 2), or only prefetched into L2 then and loaded afterwards
-        // (PF == 1: no registers held across the row); the row after it is
-        // prefetched into L2 as well, so two rows per group are in flight.
+        // (PF == 1: no registers held across the row).
         auto prefetch_l2 = [&](int64_t t) {
             if (t < p.T) {
 #pragma unroll
@@ -574,15 +607,58 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
                 }
             }
         };
-        if constexpr (PF == 1) prefetch_l2(b0 + stride + grp);
+        // Measured: the row after next pays for the static FP8 form only
+        // (38.7 against 40.9 us at T = H = 8192; the y form lost 5 %).
+        constexpr bool AHEAD2 = OUT == OUT_Q && !LN;
+        // The static FP8 form with multi-warp rows runs a software pipeline
+        // with one CTA barrier per row: iteration k adds up row k's total
+        // from the per-warp slots published before the barrier, forms row
+        // k + 1's h and partial sum and publishes it (the other plane of
+        // slots), starts the loads of row k + 2, then writes row k's outputs
+        // -- so the reduction's dependent chain overlaps the next row's
+        // arithmetic instead of stalling the CTA.  Measured at T = H = 8192:
+        // 34.5 against 38.7 us; the y and AdaRMSNorm forms, whose L2-only
+        // prefetch keeps them at about 60 registers, lost 9-25 % with it,
+        // and LayerNorm (three rows in flight, one barrier instead of two per
+        // row) lost 19 % at T = 16384, H = 4096.
+        constexpr bool PIPED = OUT == OUT_Q && !LN && !SUB;
+        if constexpr (PIPED) {
+            BVec<VEC> hc[VPT], hn[VPT];
+            const int64_t t0 = b0 + grp;
+            publish(phase_h(t0, hc), red_h[0]);
+            if (b0 + stride < p.T) load_row(t0 + stride, xa, false);
+            __syncthreads();
+            int par = 0;
+            for (int64_t base = b0; base < p.T; base += stride, par ^= 1) {
+                const int64_t t = base + grp;
+                const float total = gather(red_h[par]);
+                const bool more = base + stride < p.T;   // the same for the whole CTA
+                if (more) {
+                    publish(phase_h(t + stride, hn), red_h[par ^ 1]);
+                    if (base + 2 * stride < p.T) {
+                        if constexpr (AHEAD2) prefetch_l2(t + 3 * stride);
+                        load_row(t + 2 * stride, xa, false);
+                    }
+                }
+                finish(t, hc, total, par, true);
+                if (more) {
+#pragma unroll
+                    for (int k = 0; k < VPT; ++k) hc[k] = hn[k];
+                }
+                __syncthreads();
+            }
+            return;
+        }
         int par = 0;
         for (int64_t base = b0; base < p.T; base += stride, par ^= 1) {
             BVec<VEC> xn[VPT];
             const bool more = base + stride < p.T;   // the same for the whole CTA
             const int64_t tn = base + stride + grp;
-            prefetch_l2(tn + stride);
             if constexpr (PF == 2) {
+                if constexpr (AHEAD2) prefetch_l2(tn + stride);
                 if (more) load_row(tn, xn, false);
+            } else {
+                if (more) prefetch_l2(tn);
             }
             process(base + grp, par);
             if (more) {
