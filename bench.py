@@ -683,8 +683,9 @@ def run_ours(args):
         return
 
     # Roofline of the dominant kernel: the fused-residual forward timed on its
-    # own (back-to-back launches over inputs larger than L2, events around
-    # the loop); the event-split step loop is kept as `in_step`.
+    # own (a CUDA graph of back-to-back launches over inputs larger than L2,
+    # events around its replays); the event-split step loop is kept as
+    # `in_step_us`.
     fwd_in_step_us = fwd_us
     if fwd_alone is not None:
         fwd_us = fwd_alone["us"]
@@ -707,7 +708,8 @@ def run_ours(args):
                      "achieved": round(fwd_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(fwd_gbs / peak, 4), "peak_kind": peak_kind + " hbm_gbs",
                      "bytes_per_launch": FWD_BYTES, "us_per_launch": round(fwd_us, 2),
-                     "timing": ("standalone: back-to-back launches, events around the loop"
+                     "timing": ("standalone: a CUDA graph of back-to-back launches over inputs "
+                                "larger than L2, events around its replays"
                                 if fwd_alone is not None else "event-split step loop"),
                      "in_step_us": round(fwd_in_step_us, 2),
                      "traffic": ncu_traffic("rmsnorm_fwd")},
