@@ -342,7 +342,8 @@ def other_kernels(dev, peak, only=None):
             dx, dw = torch.empty_like(x), torch.empty(Hz, device=dev)
             ws = crm.rmsnorm_bwd_workspace(Tz, Hz, dev)
             return lambda: crm.rmsnorm_bwd(g, x, w, rstd, 1.0, dx=dx, dw=dw, workspace=ws)
-        add(f"rmsnorm_bwd FP32 zero-centred weight T={Tz} H=5120 (dx + dw, two launches)", zc_bwd,
+        form = "one launch, column form" if Tz <= 2048 else "two launches"
+        add(f"rmsnorm_bwd FP32 zero-centred weight T={Tz} H=5120 (dx + dw, {form})", zc_bwd,
             3 * Tz * Hz * 2 + Tz * 4 + 2 * Hz * 4)
 
     # The [2048, 32, 128] row-strided view of a [2048, 32, 256] buffer:

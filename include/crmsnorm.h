@@ -139,11 +139,16 @@ crmsn_status rmsnorm_fwd(const void *x, int64_t ldx,
  * inputs.  g, x, g_residual, dx: BF16 [T, H] with row strides.  w as in
  * rmsnorm_fwd.  dw: FP32 [H].  In place: dx == g (lddx == ldg) is allowed.
  *
- * dw is reduced deterministically: rows are cut into a fixed table of
- * contiguous chunks (a function of T and the device's SM count), each chunk
- * sums its rows in a fixed order with compensated FP32 sums into the
- * workspace, and a second kernel adds the chunk sums in a fixed order.  The
- * same T on devices with the same SM count gives the same dw bits.
+ * dw is reduced deterministically.  Up to 2048 rows (the column form, one
+ * launch): fixed strips of columns are each summed over all rows in a fixed
+ * order with compensated FP32 sums, the order depending only on T, H and the
+ * access width (the 16-byte or the 4-byte path), not on the SM count; the
+ * workspace is not touched.  Above 2048 rows: rows are cut into a fixed
+ * table of contiguous chunks (a function of T and the device's SM count),
+ * each chunk sums its rows in a fixed order with compensated FP32 sums into
+ * the workspace, and a second kernel adds the chunk sums in a fixed order,
+ * so the same T on devices with the same SM count gives the same dw bits.
+ * dx does not depend on the form or the chunk table.
  * workspace: caller-owned device memory of at least
  * rmsnorm_bwd_workspace_bytes() bytes, 256-byte aligned, any initial
  * content; it is scratch only and may be reused by any later call on the

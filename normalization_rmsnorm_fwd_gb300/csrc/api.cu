@@ -391,7 +391,10 @@ crmsn_status rmsnorm_bwd(const void *g, int64_t ldg, const void *x, int64_t ldx,
     p.gres = static_cast<const uint16_t *>(g_residual); p.ldgr = ldgr;
     p.dx = static_cast<uint16_t *>(dx); p.lddx = lddx;
     p.part = static_cast<float *>(workspace);
+    p.dw = dw;
     p.T = T; p.H = (int)H; p.tpr = L.tpr; p.rpc = L.rpc;
+    p.colw = bwd_column_width(T, H, vec, L.tpr * L.rpc);
+    p.ncols = p.colw > 0 ? (int)((H + p.colw - 1) / p.colw) : 0;
     return launched(launch_bwd(p, w_dtype == CRMSN_F32, g_residual != nullptr, L, sm_count(dev),
                                dw, stream));
 }

@@ -29,6 +29,13 @@
 // (bwd_reduce.cu) adds the partial rows of each column in a fixed order.
 // Both grids are launched with programmatic dependent launch and wait for
 // the preceding grid before touching global memory.
+//
+// Short inputs (the column form, the pages' "column task" for small T): the
+// same launch also carries ncols CTAs that each own a strip of colw columns
+// and add g*x*rstd over every row of the strip in a fixed order, writing dw
+// directly; the row chunks then only write dx, and no partial rows, workspace
+// or second kernel are used.  The order of the dw sum depends on T, H and the
+// layout only, so dw no longer depends on the SM count.
 #pragma once
 
 #include <atomic>
@@ -94,6 +101,120 @@ __host__ __device__ constexpr int bwd_stage_bytes(int nt, int vpt, int vec, int 
     return nt * vpt * threads * vec * 2;
 }
 
+// VEC BF16 values through L2 only (the row chunks of the same launch may
+// read them again).
+template <int VEC>
+__device__ __forceinline__ BVec<VEC> ld_l2(const uint16_t *p)
+{
+    BVec<VEC> v;
+    if constexpr (VEC == 8)
+        asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                     : "l"(p));
+    else
+        asm volatile("ld.global.cg.u32 %0, [%1];" : "=r"(v.w[0]) : "l"(p));
+    return v;
+}
+
+// Rows in flight per thread in the column form.
+constexpr int kColUnroll = 8;
+
+// Column form: dw of strip `strip` (columns [strip*colw, strip*colw + colw)
+// clipped to H) over all T rows.  A row's strip is read by colw/VEC
+// consecutive lanes (one vector each), so a warp covers 32*VEC/colw rows per
+// access and the CTA `slots` rows; row slot k takes rows k, k + slots, ...
+// in order.  Each lane adds its rows' terms (g*x)*rstd -- g*x exact from the
+// mixed-precision FMA -- into plain FP32 block sums folded into compensated
+// pairs every kDwBlock rows, as the row chunks do.  The slots of a warp are
+// then added in a butterfly (slot order fixed by the lane bits), and the
+// warps' pairs in warp order by one thread per column.  Every step depends on
+// T, H, colw and the block size only.  `scratch` holds warps x colw pairs.
+template <int VEC>
+__device__ void dw_columns(const BwdParams &p, int strip, float2 *scratch)
+{
+    constexpr int NW = VEC / 2;
+    const int lpr = p.colw / VEC;                 // lanes per row strip (power of two <= 32)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int slots = nwarps * (32 / lpr);
+    const int slot = warp * (32 / lpr) + lane / lpr;
+    const int64_t col = (int64_t)strip * p.colw + (int64_t)(lane & (lpr - 1)) * VEC;
+    const bool live = col < p.H;
+
+    float acc[VEC], cmp[VEC];
+    F2 blk[NW];
+#pragma unroll
+    for (int i = 0; i < VEC; ++i) { acc[i] = 0.f; cmp[i] = 0.f; }
+#pragma unroll
+    for (int i = 0; i < NW; ++i) blk[i] = f2(0.f);
+    auto fold = [&]() {
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+            const float b = (i & 1) ? f2_hi(blk[i >> 1]) : f2_lo(blk[i >> 1]);
+            float s2, err;
+            two_sum(acc[i], b, s2, err);
+            acc[i] = s2;
+            cmp[i] = __fadd_rn(cmp[i], err);
+        }
+#pragma unroll
+        for (int i = 0; i < NW; ++i) blk[i] = f2(0.f);
+    };
+
+    if (live) {
+        const uint16_t *gp = p.g + (int64_t)slot * p.ldg + col;
+        const uint16_t *xp = p.x + (int64_t)slot * p.ldx + col;
+        const int64_t gstep = (int64_t)slots * p.ldg, xstep = (int64_t)slots * p.ldx;
+        int n = 0;                                // rows added since the last fold
+        for (int64_t t = slot; t < p.T; t += (int64_t)kColUnroll * slots) {
+            BVec<VEC> gv[kColUnroll], xv[kColUnroll];
+            float rs[kColUnroll];
+#pragma unroll
+            for (int u = 0; u < kColUnroll; ++u) {
+                if (t + (int64_t)u * slots < p.T) {
+                    gv[u] = ld_l2<VEC>(gp + u * gstep);
+                    xv[u] = ld_l2<VEC>(xp + u * xstep);
+                    rs[u] = __ldg(p.rstd + t + (int64_t)u * slots);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kColUnroll; ++u) {
+                if (t + (int64_t)u * slots < p.T) {
+                    const F2 rs2 = f2(rs[u]);
+#pragma unroll
+                    for (int e = 0; e < NW; ++e)
+                        blk[e] = f2_fma(mul_bf16x2(gv[u].w[e], xv[u].w[e]), rs2, blk[e]);
+                    if (++n == kDwBlock) { fold(); n = 0; }
+                }
+            }
+            gp += kColUnroll * gstep;
+            xp += kColUnroll * xstep;
+        }
+    }
+    fold();
+
+    // Slots of the warp: partners differ in one slot bit and add each
+    // other's pairs (pair_add is symmetric, so both hold the same bits).
+    for (int o = lpr; o < 32; o <<= 1)
+#pragma unroll
+        for (int i = 0; i < VEC; ++i) {
+            const float bh = __shfl_xor_sync(0xffffffffu, acc[i], o);
+            const float bl = __shfl_xor_sync(0xffffffffu, cmp[i], o);
+            pair_add(acc[i], cmp[i], bh, bl);
+        }
+    if (lane < lpr)
+#pragma unroll
+        for (int i = 0; i < VEC; ++i)
+            scratch[warp * p.colw + lane * VEC + i] = make_float2(acc[i], cmp[i]);
+    __syncthreads();
+    for (int c = threadIdx.x; c < p.colw; c += blockDim.x) {
+        const int64_t j = (int64_t)strip * p.colw + c;
+        if (j >= p.H) continue;
+        float h = scratch[c].x, l = scratch[c].y;
+        for (int w = 1; w < nwarps; ++w) pair_add(h, l, scratch[w * p.colw + c].x, scratch[w * p.colw + c].y);
+        p.dw[j] = __fadd_rn(h, l);
+    }
+}
+
 template <bool W32, bool GRES, int VEC, int VPT, bool SUB, int D>
 __global__ void __launch_bounds__(kBwdMaxThreads, 1)
 k_rmsnorm_bwd(const BwdParams p)
@@ -115,14 +236,21 @@ k_rmsnorm_bwd(const BwdParams p)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+    // Column form: the first ncols CTAs each reduce one strip of dw.
+    if ((int)blockIdx.x < p.ncols) {
+        dw_columns<VEC>(p, blockIdx.x, reinterpret_cast<float2 *>(dyn_smem));
+        return;
+    }
+    const int chunk = blockIdx.x - p.ncols;
+
     const int nthr = blockDim.x;
     const int tpr = p.tpr;
     const int rpc = p.rpc;
     const int grp = row_group(tpr, p.rpc);
     const int lane = threadIdx.x - grp * tpr;
     const int nvec = p.H / VEC;
-    const int64_t r0 = (int64_t)blockIdx.x * p.T / p.nchunk;
-    const int64_t r1 = (int64_t)(blockIdx.x + 1) * p.T / p.nchunk;
+    const int64_t r0 = (int64_t)chunk * p.T / p.nchunk;
+    const int64_t r1 = (int64_t)(chunk + 1) * p.T / p.nchunk;
     const int64_t iters = (r1 - r0 + rpc - 1) / rpc;
 
     // Shared memory: ring [S][stage], then w_eff [VPT*tpr*VEC] (zero past H),
@@ -495,13 +623,14 @@ k_rmsnorm_bwd(const BwdParams p)
     }
     fold();
     cp_async_wait<0>();
+    if (p.ncols > 0) return;                 // dw comes from the column CTAs
 
     // Combine the CTA's row groups in group order, then write the partial row.
     // With several groups, every group stores its (sum, compensation) pairs in
     // comb[group][column], and after one barrier each thread adds whole
     // columns over the groups in group order (the same order, so the same
     // bits, as one group adding the others in turn, but spread over the CTA).
-    float *prow = p.part + (int64_t)blockIdx.x * p.H;
+    float *prow = p.part + (int64_t)chunk * p.H;
     if (rpc > 1) {
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
@@ -580,15 +709,24 @@ struct BwdInst {
         return cudaSuccess;
     }
 
+    // Row chunks: as many as resident CTAs (per_sm x SMs) less the strip
+    // CTAs, but at least a third of the resident CTAs, and at most one chunk
+    // per row group.  Strip and chunk CTAs run side by side: a strip CTA
+    // reads 4 bytes per row and column of its strip, a chunk CTA 6 (8 with
+    // g_residual) per row and column of its rows.
     static cudaError_t launch(BwdParams p, int per_sm, int sms, int *nchunk_out, cudaStream_t s)
     {
         const int threads = p.tpr * p.rpc;
-        const size_t smem = bwd_smem_bytes(GRES, VEC, VPT, threads, p.rpc, p.H, D);
+        size_t smem = bwd_smem_bytes(GRES, VEC, VPT, threads, p.rpc, p.H, D);
+        const size_t col_smem = (size_t)(threads / 32) * p.colw * sizeof(float2);
+        if (p.ncols > 0 && col_smem > smem) smem = col_smem;
         const int64_t by_rows = (p.T + p.rpc - 1) / p.rpc;
-        const int64_t cap = (int64_t)per_sm * sms;
+        const int64_t resident = (int64_t)per_sm * sms;
+        int64_t cap = resident - p.ncols;
+        if (cap < (resident + 2) / 3) cap = (resident + 2) / 3;
         p.nchunk = (int)(by_rows < cap ? by_rows : cap);
         *nchunk_out = p.nchunk;
-        return launch_pdl(kern, dim3((unsigned)p.nchunk), dim3(threads), smem, s, p);
+        return launch_pdl(kern, dim3((unsigned)(p.ncols + p.nchunk)), dim3(threads), smem, s, p);
     }
 };
 

@@ -1,6 +1,8 @@
 // bwd_reduce.cu -- the fixed-order reduction of the backward's per-chunk dw
 // partial rows, and the backward launch sequence (partials kernel, then this
-// reduction; every launch uses programmatic dependent launch).
+// reduction; every launch uses programmatic dependent launch).  In the
+// column form the backward kernel writes dw itself and this reduction is not
+// launched.
 #include "launch.h"
 
 namespace crmsn {
@@ -67,7 +69,7 @@ cudaError_t launch_bwd(BwdParams p, bool w32, bool gres, const Layout &L, int sm
                                 : launch_bwd_f32w_plain(p, L, sms, &nchunk, s))
                         : (gres ? launch_bwd_bf16w_gres(p, L, sms, &nchunk, s)
                                 : launch_bwd_bf16w_plain(p, L, sms, &nchunk, s));
-    if (e != cudaSuccess) return e;
+    if (e != cudaSuccess || p.ncols > 0) return e;
     return launch_dw_reduce(p.part, nchunk, p.H, dw, s);
 }
 

@@ -76,9 +76,31 @@ struct BwdParams {
     const uint16_t *gres; int64_t ldgr;
     uint16_t *dx;        int64_t lddx;
     float *part;                          // [nchunk][H] partial dw rows
+    float *dw;                            // [H], written by the column CTAs
     int64_t T;           int H;
     int nchunk;          int tpr;         int rpc;
+    int ncols;           int colw;        // column form: strips and their width (0: off)
 };
+
+// Column form of the backward's dw (bwd.cuh): used when T is at most
+// kBwdColumnRows.  Strips of colw columns: the widest power of two in
+// [16, 256] (16-byte accesses; [16, 64] for 4-byte ones) that still gives at
+// least `strips` strips (else 16).  A strip CTA reads 4 bytes per row and
+// column, a row CTA 6 per row and column of its chunk, so about 0.4 of the
+// resident CTAs should take strips: 128 strips when the layout's CTA (of
+// `threads` threads) fits twice on an SM, 64 when it fits once (more than
+// 256 threads).  A function of T, H and the layout only, like the sum's
+// order.
+constexpr int64_t kBwdColumnRows = 2048;
+inline int bwd_column_width(int64_t T, int64_t H, int vec, int threads)
+{
+    if (T > kBwdColumnRows) return 0;
+    const int top = vec == 8 ? 256 : 64;
+    const int strips = threads > 256 ? 64 : 128;
+    int cw = 16;
+    while (cw < top && (H + 2 * cw - 1) / (2 * cw) >= strips) cw *= 2;
+    return cw;
+}
 
 // Row layout picked by the host: VEC elements per access, VPT accesses per
 // thread, tpr threads per row (SUB: a power of two <= 32), rpc rows per CTA.
@@ -167,7 +189,8 @@ cudaError_t launch_fwd_layernorm(const FwdParams &p, int fp8k, const Layout &L, 
 // Backward (bwd.cu).
 // Picks the chunk count (resident CTAs per SM x sms, at most
 // kBwdMaxCtasPerSm x sms and at most one per row group), launches the dx /
-// partial-dw kernel and then the fixed-order dw reduction (bwd_reduce.cu).
+// partial-dw kernel and then the fixed-order dw reduction (bwd_reduce.cu);
+// with p.ncols > 0 (the column form) one launch writes dx and dw.
 cudaError_t launch_bwd(BwdParams p, bool w32, bool gres, const Layout &L, int sms, float *dw,
                        cudaStream_t s);
 // The dx / partial-dw kernel alone, per weight type and g_residual

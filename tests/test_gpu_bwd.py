@@ -65,11 +65,13 @@ def test_plain_small_config(orc):
 
 # 8192 with g_residual, 9002 with g_residual (4-byte path) and 12288 run the
 # backward with two rows in flight (three ring stages fit, four do not).
+# 300 rows take dw from the column CTAs, 2500 rows from the chunks' partial
+# rows and the reduction kernel.
 @pytest.mark.parametrize("H", [2, 8, 64, 128, 200, 256, 520, 1024, 2048, 3072, 4096, 5120,
                                6144, 8192, 9002, 12288, 16384])
 @pytest.mark.parametrize("route", ["bf16", "f32", "bf16_gres"])
-def test_widths_and_routes(orc, H, route):
-    T = 300
+@pytest.mark.parametrize("T", [300, 2500])
+def test_widths_and_routes(orc, H, route, T):
     g, x, gr = synth.random_rows(H + 3, T, H, n=3)
     f32 = route == "f32"
     w = synth.random_weight(H + 4, H, f32=f32)
@@ -119,13 +121,15 @@ def test_strided_heads_config(orc):
                     dw.cpu().numpy(), bias=1.0)
 
 
-def test_dw_is_bitwise_reproducible():
+@pytest.mark.parametrize("T", [1000, 16384])
+def test_dw_is_bitwise_reproducible(T):
     """Three runs, and a run on a second stream with a reused workspace, give
-    identical dw and dx bits."""
-    g, x = synth.random_rows(21, 16384, 4096, n=2)
+    identical dw and dx bits (1000 rows: the column form; 16384: the chunk
+    table)."""
+    g, x = synth.random_rows(21, T, 4096, n=2)
     w = synth.random_weight(21, 4096)
-    rstd = np.abs(synth.Draw(21).f32((16384,), 0.1, 1.0))
-    ws = crm.rmsnorm_bwd_workspace(16384, 4096, gu.DEV)
+    rstd = np.abs(synth.Draw(21).f32((T,), 0.1, 1.0))
+    ws = crm.rmsnorm_bwd_workspace(T, 4096, gu.DEV)
     runs = [run_bwd(g, x, w, rstd, workspace=ws) for _ in range(3)]
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
@@ -177,13 +181,14 @@ def test_dx_in_place_over_g(orc):
 
 
 @pytest.mark.parametrize("H", [1024, 4096])
-@pytest.mark.parametrize("T", [305, 608, 913, 1500, 2431])
+@pytest.mark.parametrize("T", [305, 608, 913, 1500, 2048, 2049, 2431])
 def test_pipelined_chunk_lengths(orc, H, T):
     # Multi-warp rows run the software-pipelined loop (row i+1's sum formed
     # while row i's dx is written); these row counts give chunks of one to
     # eight rows, so the prologue, the steady state and the tail (rows past
     # the chunk) all occur, with one and two row groups per CTA (H = 4096 and
-    # H = 1024).
+    # H = 1024).  Up to 2048 rows dw comes from the column CTAs of the same
+    # launch, above it from the chunks' partial rows.
     g, x = synth.random_rows(T + H, T, H, n=2)
     w = synth.random_weight(T + 7, H)
     compare(orc, g, x, w)
