@@ -74,7 +74,8 @@ typedef enum crmsn_status {
     CRMSN_ERR_CUDA = 8,           /* the CUDA runtime reported an error */
     CRMSN_ERR_DEVICE_TIMEOUT = 9, /* reserved: the kernels have no device-side waits */
     CRMSN_ERR_ARG = 10,           /* eps / scale value out of range */
-    CRMSN_ERR_SCRATCH_LIMIT = 11  /* rmsnorm_bwd_noalloc: problem needs more than its built-in scratch */
+    CRMSN_ERR_SCRATCH_LIMIT = 11, /* rmsnorm_bwd_noalloc: problem needs more than its built-in scratch */
+    CRMSN_ERR_NOT_DEBUG_BUILD = 12 /* crmsn_debug_status: the library has no bounds guard */
 } crmsn_status;
 
 /* Weight storage types. */
@@ -348,6 +349,23 @@ crmsn_status layernorm_quant(void *out, int64_t ldo, int fp8_kind,
                              const float *scale, float eps,
                              int64_t T, int64_t H, float *mean, float *rstd,
                              cudaStream_t stream);
+
+/*
+ * crmsn_debug_status -- no counterpart on the pages: the bounds guard of the
+ * debug build (compiled with -DCRMSN_DEBUG; build.py's debug option).  In
+ * that build every global load and store of every kernel is checked against
+ * the byte ranges of the call's tensors (all readable; outputs and the
+ * workspace writable) and every dynamic shared-memory access against the
+ * launch's size; an access outside them is skipped (a load reads zeros) and
+ * the first one is recorded.  This call waits for the device
+ * (cudaDeviceSynchronize), stores the recorded word in *violation (0 when
+ * every access was in bounds; otherwise bit 63 set, bits 62..56 the kind --
+ * 1 load, 2 store, 3 asynchronous copy, 4 shared memory -- bits 55..32 the
+ * CTA, 31..22 the thread, 21..0 the low bits of the global address or of
+ * the shared-memory byte offset) and clears it.  The
+ * normal build stores 0 and returns CRMSN_ERR_NOT_DEBUG_BUILD.
+ */
+crmsn_status crmsn_debug_status(uint64_t *violation);
 
 /*
  * rmsnorm_supports -- [API] supports_* helpers; [GUIDE] 6.1

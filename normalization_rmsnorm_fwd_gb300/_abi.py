@@ -34,13 +34,14 @@ SIGNATURES = {
     "fused_rmsnorm_silu": (_ST, [_P, _I, _INT, _P, _I, _P, _INT, _F, _P, _F, _I, _I, _P, _P]),
     "layernorm": (_ST, [_P, _I, _P, _I, _P, _P, _F, _I, _I, _P, _P, _P]),
     "layernorm_quant": (_ST, [_P, _I, _INT, _P, _I, _P, _P, _P, _F, _I, _I, _P, _P, _P]),
+    "crmsn_debug_status": (_ST, [ctypes.POINTER(ctypes.c_uint64)]),
 }
 
 STATUS = {
     0: "CRMSN_OK", 1: "CRMSN_ERR_NULL", 2: "CRMSN_ERR_SHAPE", 3: "CRMSN_ERR_UNSUPPORTED_H",
     4: "CRMSN_ERR_ALIGNMENT", 5: "CRMSN_ERR_DTYPE", 6: "CRMSN_ERR_WORKSPACE",
     7: "CRMSN_ERR_ALIAS", 8: "CRMSN_ERR_CUDA", 9: "CRMSN_ERR_DEVICE_TIMEOUT", 10: "CRMSN_ERR_ARG",
-    11: "CRMSN_ERR_SCRATCH_LIMIT",
+    11: "CRMSN_ERR_SCRATCH_LIMIT", 12: "CRMSN_ERR_NOT_DEBUG_BUILD",
 }
 OK = 0
 BF16, F32 = 0, 1

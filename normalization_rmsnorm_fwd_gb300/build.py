@@ -4,7 +4,10 @@ Every ``csrc/*.cu`` is compiled in parallel to an object file under
 ``_build/`` and the objects are linked into one shared library
 (CUDA runtime linked statically).  A stamp of the sources and flags skips
 the build when nothing changed.  Run ``python -m
-normalization_rmsnorm_fwd_gb300.build [-v]`` (``-v`` adds ``-Xptxas -v``).
+normalization_rmsnorm_fwd_gb300.build [-v] [--debug]`` (``-v`` adds
+``-Xptxas -v``; ``--debug`` builds ``_build_debug/libcrmsnorm_debug.so``
+with ``-DCRMSN_DEBUG``: the kernels' bounds guard, read back with
+``crmsn_debug_status``).
 """
 from __future__ import annotations
 
@@ -21,6 +24,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "libcrmsnorm.so")
+OUT_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(OUT_DEBUG, "libcrmsnorm_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # Hidden symbols: the shared library exports only the C ABI of crmsnorm.h,
@@ -52,17 +57,18 @@ def _stamp(extra) -> str:
     return h.hexdigest()
 
 
-def build(verbose: bool = False, force: bool = False) -> str:
-    extra = ["-Xptxas", "-v"] if verbose else []
-    os.makedirs(OUT, exist_ok=True)
-    stamp_path = os.path.join(OUT, "stamp")
+def build(verbose: bool = False, force: bool = False, debug: bool = False) -> str:
+    extra = (["-Xptxas", "-v"] if verbose else []) + (["-DCRMSN_DEBUG"] if debug else [])
+    out, lib = (OUT_DEBUG, LIB_DEBUG) if debug else (OUT, LIB)
+    os.makedirs(out, exist_ok=True)
+    stamp_path = os.path.join(out, "stamp")
     stamp = _stamp(extra)
-    if (not force and os.path.exists(LIB) and os.path.exists(stamp_path)
+    if (not force and os.path.exists(lib) and os.path.exists(stamp_path)
             and open(stamp_path).read() == stamp):
-        return LIB
+        return lib
     nvcc = _nvcc()
     srcs = _sources()
-    objs = [os.path.join(OUT, os.path.basename(s)[:-3] + ".o") for s in srcs]
+    objs = [os.path.join(out, os.path.basename(s)[:-3] + ".o") for s in srcs]
 
     def compile_one(src_obj):
         src, obj = src_obj
@@ -79,15 +85,15 @@ def build(verbose: bool = False, force: bool = False) -> str:
                 failed.append(src)
     if failed:
         raise RuntimeError(f"nvcc failed for {failed}")
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
     if r.returncode:
         raise RuntimeError("link failed:\n" + r.stdout + r.stderr)
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp_path, "w") as f:
         f.write(stamp)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv))
+    print(build(verbose="-v" in sys.argv, force="-f" in sys.argv, debug="--debug" in sys.argv))

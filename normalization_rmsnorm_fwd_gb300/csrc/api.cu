@@ -4,6 +4,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 
 #include "crmsnorm.h"
@@ -239,6 +240,68 @@ crmsn_status check_h(int64_t H)
 
 constexpr int64_t kMaxBlocks = 0x7fffffff;
 
+#ifdef CRMSN_DEBUG
+// The debug build's violation word (one per device; its address is looked up
+// once per device) and the range table of a call: every tensor of the call,
+// the outputs writable.
+__device__ unsigned long long g_debug_word;
+constexpr int kDebugDevices = 64;
+std::mutex g_debug_mutex;
+unsigned long long *g_debug_word_ptr[kDebugDevices];
+
+unsigned long long *debug_word()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDebugDevices) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_debug_mutex);
+    if (!g_debug_word_ptr[dev]) {
+        void *a = nullptr;
+        if (cudaGetSymbolAddress(&a, g_debug_word) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        g_debug_word_ptr[dev] = static_cast<unsigned long long *>(a);
+    }
+    return g_debug_word_ptr[dev];
+}
+
+template <int N>
+DebugRanges debug_ranges(const Tensor (&ts)[N])
+{
+    static_assert(N <= kDebugMaxRanges, "more tensors than debug ranges");
+    DebugRanges d{};
+    d.word = debug_word();
+    for (int i = 0; i < N; ++i) {
+        const Region &r = ts[i].r;
+        if (!r.p || r.rows == 0) continue;
+        const uintptr_t a = (uintptr_t)r.p;
+        d.lo[d.n] = a;
+        d.hi[d.n] = a + (uintptr_t)(((r.rows - 1) * r.ld + r.cols) * r.es);
+        if (ts[i].out) d.writable |= 1u << d.n;
+        ++d.n;
+    }
+    // Self-test of the guard: CRMSN_DEBUG_TRIM_OUTPUT=k takes k bytes off
+    // the end of the first output's range (the guard's view only: the
+    // buffer itself is untouched), so the stores there are reported and
+    // skipped.
+    if (const char *t = getenv("CRMSN_DEBUG_TRIM_OUTPUT")) {
+        const unsigned long long k = strtoull(t, nullptr, 10);
+        for (int i = 0; i < d.n; ++i)
+            if ((d.writable >> i) & 1u) {
+                d.hi[i] = d.hi[i] - k > d.lo[i] ? d.hi[i] - k : d.lo[i];
+                break;
+            }
+    }
+    return d;
+}
+#define CRMSN_SET_DEBUG(p, ts) ((p).dbg = debug_ranges(ts))
+#else
+#define CRMSN_SET_DEBUG(p, ts) ((void)0)
+#endif
+
 }  // namespace
 
 // ======================================================================
@@ -259,8 +322,30 @@ const char *crmsn_status_str(crmsn_status s)
         case CRMSN_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
         case CRMSN_ERR_ARG: return "eps or scale out of range";
         case CRMSN_ERR_SCRATCH_LIMIT: return "problem needs more than the built-in 16 MiB backward scratch";
+        case CRMSN_ERR_NOT_DEBUG_BUILD: return "this library was built without the debug bounds guard";
     }
     return "unknown status";
+}
+
+crmsn_status crmsn_debug_status(uint64_t *violation)
+{
+    if (!violation) return CRMSN_ERR_NULL;
+    *violation = 0;
+#ifdef CRMSN_DEBUG
+    if (!debug_word()) return CRMSN_ERR_CUDA;
+    unsigned long long w = 0;
+    const unsigned long long zero = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpyFromSymbol(&w, g_debug_word, sizeof w) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_debug_word, &zero, sizeof zero) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return CRMSN_ERR_CUDA;
+    }
+    *violation = w;
+    return CRMSN_OK;
+#else
+    return CRMSN_ERR_NOT_DEBUG_BUILD;
+#endif
 }
 
 crmsn_status rmsnorm_supports(int64_t H, int w_dtype, int op)
@@ -321,6 +406,7 @@ crmsn_status rmsnorm_fwd(const void *x, int64_t ldx, const void *residual, int64
     if ((T + L.rpc - 1) / L.rpc > kMaxBlocks) return CRMSN_ERR_SHAPE;
 
     FwdParams p{};
+    CRMSN_SET_DEBUG(p, ts);
     p.x = static_cast<const uint16_t *>(x); p.ldx = ldx;
     p.r = static_cast<const uint16_t *>(residual); p.ldr = ldr;
     p.w = w; p.bias = weight_bias; p.eps = eps;
@@ -385,6 +471,7 @@ crmsn_status rmsnorm_bwd(const void *g, int64_t ldg, const void *x, int64_t ldx,
     const Layout L = choose_bwd((int)H, vec);
 
     BwdParams p{};
+    CRMSN_SET_DEBUG(p, ts);
     p.g = static_cast<const uint16_t *>(g); p.ldg = ldg;
     p.x = static_cast<const uint16_t *>(x); p.ldx = ldx;
     p.w = w; p.bias = weight_bias; p.rstd = rstd;
@@ -431,6 +518,7 @@ crmsn_status fused_add_rmsnorm_quant(void *out, int64_t ldo, int fp8_kind, const
     if ((T + L.rpc - 1) / L.rpc > kMaxBlocks) return CRMSN_ERR_SHAPE;
 
     FwdParams p{};
+    CRMSN_SET_DEBUG(p, ts);
     p.x = static_cast<const uint16_t *>(x); p.ldx = ldx;
     p.r = static_cast<const uint16_t *>(residual); p.ldr = ldr;
     p.w = w; p.bias = weight_bias; p.eps = eps;
@@ -473,6 +561,7 @@ crmsn_status fused_add_rmsnorm_fp8_block_quant(void *out, float *block_scale, in
     if ((T + L.rpc - 1) / L.rpc > kMaxBlocks) return CRMSN_ERR_SHAPE;
 
     FwdParams p{};
+    CRMSN_SET_DEBUG(p, ts);
     p.x = static_cast<const uint16_t *>(x); p.ldx = ldx;
     p.r = static_cast<const uint16_t *>(residual); p.ldr = ldr;
     p.w = w; p.bias = 0.f; p.eps = eps;
@@ -518,6 +607,7 @@ static crmsn_status ada_common(void *residual, const void *x, const void *gate, 
     if ((T + L.rpc - 1) / L.rpc > kMaxBlocks) return CRMSN_ERR_SHAPE;
 
     FwdParams p{};
+    CRMSN_SET_DEBUG(p, ts);
     p.x = static_cast<const uint16_t *>(x); p.ldx = D;
     p.r = static_cast<const uint16_t *>(residual); p.ldr = D;
     p.gate = static_cast<const uint16_t *>(gate); p.ldgate = D;
@@ -581,6 +671,7 @@ crmsn_status fused_rmsnorm_silu(void *out, int64_t ldo, int out_format, const vo
     if ((T + L.rpc - 1) / L.rpc > kMaxBlocks) return CRMSN_ERR_SHAPE;
 
     FwdParams p{};
+    CRMSN_SET_DEBUG(p, ts);
     p.x = static_cast<const uint16_t *>(x); p.ldx = ldx;
     p.w = w; p.bias = weight_bias; p.eps = eps;
     p.T = T; p.H = (int)H;
@@ -630,6 +721,7 @@ crmsn_status layernorm_common(void *out, int64_t ldo, int fp8k, const void *x, i
     if ((T + L.rpc - 1) / L.rpc > kMaxBlocks) return CRMSN_ERR_SHAPE;
 
     FwdParams p{};
+    CRMSN_SET_DEBUG(p, ts);
     p.x = static_cast<const uint16_t *>(x); p.ldx = ldx;
     p.w = gamma; p.beta = beta; p.eps = eps;
     p.T = T; p.H = (int)H;

@@ -44,15 +44,23 @@
 
 namespace crmsn {
 
+#ifdef CRMSN_DEBUG
+constexpr unsigned DBG_ASYNC_COPY_KIND = DBG_ASYNC_COPY;
+#else
+constexpr unsigned DBG_ASYNC_COPY_KIND = 0;
+#endif
+
 // Per-thread asynchronous global -> shared copies.
 __device__ __forceinline__ void cp_async_16(void *smem, const void *gmem)
 {
+    if (!dbg_shared(smem, 16) || !dbg_global(gmem, 16, false, DBG_ASYNC_COPY_KIND)) return;
     const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(s), "l"(gmem) : "memory");
 }
 
 __device__ __forceinline__ void cp_async_4(void *smem, const void *gmem)
 {
+    if (!dbg_shared(smem, 4) || !dbg_global(gmem, 4, false, DBG_ASYNC_COPY_KIND)) return;
     const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(s), "l"(gmem) : "memory");
 }
@@ -71,6 +79,10 @@ template <int VEC>
 __device__ __forceinline__ BVec<VEC> ld_smem_vec(const unsigned char *p)
 {
     BVec<VEC> v;
+    if (!dbg_shared(p, VEC * 2)) {
+        for (int i = 0; i < VEC / 2; ++i) v.w[i] = 0u;
+        return v;
+    }
     if constexpr (VEC == 8) {
         const uint4 u = *reinterpret_cast<const uint4 *>(p);
         v.w[0] = u.x; v.w[1] = u.y; v.w[2] = u.z; v.w[3] = u.w;
@@ -80,19 +92,19 @@ __device__ __forceinline__ BVec<VEC> ld_smem_vec(const unsigned char *p)
     return v;
 }
 
-// VEC FP32 values from shared memory as VEC/2 pairs, in 16-byte (8-byte)
-// accesses.
-template <int VEC>
-__device__ __forceinline__ void ld_smem_f2(const float *p, F2 (&f)[VEC / 2])
+// One FP32 value, and one (sum, compensation) pair, in shared memory.
+__device__ __forceinline__ void st_smem_f32(float *p, float v)
 {
-    if constexpr (VEC == 8) {
-        const float4 a = *reinterpret_cast<const float4 *>(p);
-        const float4 b = *reinterpret_cast<const float4 *>(p + 4);
-        f[0] = f2(a.x, a.y); f[1] = f2(a.z, a.w); f[2] = f2(b.x, b.y); f[3] = f2(b.z, b.w);
-    } else {
-        const float2 a = *reinterpret_cast<const float2 *>(p);
-        f[0] = f2(a.x, a.y);
-    }
+    if (dbg_shared(p, 4)) *p = v;
+}
+__device__ __forceinline__ void st_smem_pair(float *p, float h, float l)
+{
+    if (dbg_shared(p, 8)) *reinterpret_cast<float2 *>(p) = make_float2(h, l);
+}
+__device__ __forceinline__ float2 ld_smem_pair(const float *p)
+{
+    if (!dbg_shared(p, 8)) return make_float2(0.f, 0.f);
+    return *reinterpret_cast<const float2 *>(p);
 }
 
 // Bytes of one ring stage: NT tensors x VPT vectors per thread.
@@ -107,6 +119,10 @@ template <int VEC>
 __device__ __forceinline__ BVec<VEC> ld_l2(const uint16_t *p)
 {
     BVec<VEC> v;
+    if (!dbg_global(p, VEC * 2, false)) {
+        for (int i = 0; i < VEC / 2; ++i) v.w[i] = 0u;
+        return v;
+    }
     if constexpr (VEC == 8)
         asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];"
                      : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
@@ -173,7 +189,7 @@ __device__ void dw_columns(const BwdParams &p, int strip, float2 *scratch)
                 if (t + (int64_t)u * slots < p.T) {
                     gv[u] = ld_l2<VEC>(gp + u * gstep);
                     xv[u] = ld_l2<VEC>(xp + u * xstep);
-                    rs[u] = __ldg(p.rstd + t + (int64_t)u * slots);
+                    rs[u] = ld_f32_ro(p.rstd + t + (int64_t)u * slots);
                 }
             }
 #pragma unroll
@@ -204,14 +220,18 @@ __device__ void dw_columns(const BwdParams &p, int strip, float2 *scratch)
     if (lane < lpr)
 #pragma unroll
         for (int i = 0; i < VEC; ++i)
-            scratch[warp * p.colw + lane * VEC + i] = make_float2(acc[i], cmp[i]);
+            st_smem_pair(reinterpret_cast<float *>(scratch + warp * p.colw + lane * VEC + i), acc[i], cmp[i]);
     __syncthreads();
     for (int c = threadIdx.x; c < p.colw; c += blockDim.x) {
         const int64_t j = (int64_t)strip * p.colw + c;
         if (j >= p.H) continue;
-        float h = scratch[c].x, l = scratch[c].y;
-        for (int w = 1; w < nwarps; ++w) pair_add(h, l, scratch[w * p.colw + c].x, scratch[w * p.colw + c].y);
-        p.dw[j] = __fadd_rn(h, l);
+        const float2 s0 = ld_smem_pair(reinterpret_cast<const float *>(scratch + c));
+        float h = s0.x, l = s0.y;
+        for (int w = 1; w < nwarps; ++w) {
+            const float2 sw = ld_smem_pair(reinterpret_cast<const float *>(scratch + w * p.colw + c));
+            pair_add(h, l, sw.x, sw.y);
+        }
+        st_f32(p.dw + j, __fadd_rn(h, l));
     }
 }
 
@@ -235,6 +255,7 @@ k_rmsnorm_bwd(const BwdParams p)
     // (it waits for this whole grid the same way).
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    CRMSN_DEBUG_ENTER(p.dbg);
 
     // Column form: the first ncols CTAs each reduce one strip of dw.
     if ((int)blockIdx.x < p.ncols) {
@@ -276,6 +297,11 @@ k_rmsnorm_bwd(const BwdParams p)
     };
     auto ld_w = [&](int k, F2 (&we)[NW]) {
         const int v = k * tpr + lane;
+        if (VEC == 8 ? !dbg_shared(wsm + v * 4, 16) || !dbg_shared(wsm + wplane + v * 4, 16)
+                     : !dbg_shared(wsm + v * VEC, 8)) {
+            for (int e = 0; e < NW; ++e) we[e] = f2(0.f);
+            return;
+        }
         if constexpr (VEC == 8) {
             const float4 a = *reinterpret_cast<const float4 *>(wsm + v * 4);
             const float4 b = *reinterpret_cast<const float4 *>(wsm + wplane + v * 4);
@@ -339,6 +365,7 @@ k_rmsnorm_bwd(const BwdParams p)
             for (int st = 0; st < S; ++st)
 #pragma unroll
                 for (int ti = 0; ti < NT; ++ti) {
+                    if (!dbg_shared(slot(st, ti, k), VB)) continue;
                     if constexpr (VEC == 8)
                         *reinterpret_cast<uint4 *>(slot(st, ti, k)) = make_uint4(0u, 0u, 0u, 0u);
                     else
@@ -346,19 +373,19 @@ k_rmsnorm_bwd(const BwdParams p)
                 }
             if (grp == 0)
 #pragma unroll
-                for (int i = 0; i < VEC; ++i) *w_at(v, i) = 0.f;
+                for (int i = 0; i < VEC; ++i) st_smem_f32(w_at(v, i), 0.f);
         } else if (grp == 0) {
             if constexpr (W32) {
                 float f[VEC];
                 ld_f32_keep<VEC>(static_cast<const float *>(p.w) + c, f);
 #pragma unroll
-                for (int i = 0; i < VEC; ++i) *w_at(v, i) = __fadd_rn(f[i], p.bias);
+                for (int i = 0; i < VEC; ++i) st_smem_f32(w_at(v, i), __fadd_rn(f[i], p.bias));
             } else {
                 BVec<VEC> wb = ld_keep<VEC>(static_cast<const uint16_t *>(p.w) + c);
 #pragma unroll
                 for (int i = 0; i < NW; ++i) {
-                    *w_at(v, 2 * i) = __fadd_rn(bf_lo(wb.w[i]), p.bias);
-                    *w_at(v, 2 * i + 1) = __fadd_rn(bf_hi(wb.w[i]), p.bias);
+                    st_smem_f32(w_at(v, 2 * i), __fadd_rn(bf_lo(wb.w[i]), p.bias));
+                    st_smem_f32(w_at(v, 2 * i + 1), __fadd_rn(bf_hi(wb.w[i]), p.bias));
                 }
             }
         }
@@ -375,7 +402,7 @@ k_rmsnorm_bwd(const BwdParams p)
     const int bl = lane & (BL - 1);
     auto rs_block = [&](int64_t it0) -> float {
         const int64_t t = r0 + grp + (it0 + bl) * rpc;
-        return t < r1 ? __ldg(p.rstd + t) : 0.f;
+        return t < r1 ? ld_f32_ro(p.rstd + t) : 0.f;
     };
     float rs_cur = rs_block(0), rs_nxt = rs_block(BL);
     // rstd of iteration i, i in the current (it's) or the next block; called
@@ -638,18 +665,17 @@ k_rmsnorm_bwd(const BwdParams p)
             if (v < nvec)
 #pragma unroll
                 for (int i = 0; i < VEC; ++i)
-                    *reinterpret_cast<float2 *>(comb + ((int64_t)grp * p.H + (int64_t)v * VEC + i) * 2) =
-                        make_float2(acc[k][i], cmp[k][i]);
+                    st_smem_pair(comb + ((int64_t)grp * p.H + (int64_t)v * VEC + i) * 2, acc[k][i], cmp[k][i]);
         }
         __syncthreads();
         for (int col = threadIdx.x; col < p.H; col += nthr) {
-            const float2 c0 = *reinterpret_cast<const float2 *>(comb + (int64_t)col * 2);
+            const float2 c0 = ld_smem_pair(comb + (int64_t)col * 2);
             float h = c0.x, l = c0.y;
             for (int gi = 1; gi < rpc; ++gi) {
-                const float2 c = *reinterpret_cast<const float2 *>(comb + ((int64_t)gi * p.H + col) * 2);
+                const float2 c = ld_smem_pair(comb + ((int64_t)gi * p.H + col) * 2);
                 pair_add(h, l, c.x, c.y);
             }
-            prow[col] = __fadd_rn(h, l);
+            st_f32(prow + col, __fadd_rn(h, l));
         }
     } else {
 #pragma unroll
@@ -658,7 +684,7 @@ k_rmsnorm_bwd(const BwdParams p)
             if (v < nvec)
 #pragma unroll
                 for (int i = 0; i < VEC; ++i)
-                    prow[(int64_t)v * VEC + i] = __fadd_rn(acc[k][i], cmp[k][i]);
+                    st_f32(prow + (int64_t)v * VEC + i, __fadd_rn(acc[k][i], cmp[k][i]));
         }
     }
 }

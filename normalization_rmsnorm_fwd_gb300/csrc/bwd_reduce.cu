@@ -18,11 +18,20 @@ namespace crmsn {
 constexpr int kReduceWarps = 32;
 constexpr int kBatch = 16;
 
+#ifdef CRMSN_DEBUG
+#define DW_REDUCE_DEBUG_PARAM , const DebugRanges dbg
+#define DW_REDUCE_DEBUG_ARG , p.dbg
+#else
+#define DW_REDUCE_DEBUG_PARAM
+#define DW_REDUCE_DEBUG_ARG
+#endif
+
 __global__ void __launch_bounds__(32 * kReduceWarps)
-k_dw_reduce(const float *__restrict__ part, int nchunk, int H, float *__restrict__ dw)
+k_dw_reduce(const float *__restrict__ part, int nchunk, int H, float *__restrict__ dw DW_REDUCE_DEBUG_PARAM)
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    CRMSN_DEBUG_ENTER(dbg);
     __shared__ float sh_h[kReduceWarps][33], sh_l[kReduceWarps][33];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -35,7 +44,8 @@ k_dw_reduce(const float *__restrict__ part, int nchunk, int H, float *__restrict
             float v[kBatch];
 #pragma unroll
             for (int i = 0; i < kBatch; ++i)
-                v[i] = (c + i < c1) ? __ldcg(part + (int64_t)(c + i) * H + col) : 0.f;
+                v[i] = (c + i < c1 && dbg_global(part + (int64_t)(c + i) * H + col, 4, false))
+                           ? __ldcg(part + (int64_t)(c + i) * H + col) : 0.f;
 #pragma unroll
             for (int i = 0; i < kBatch; ++i) {
                 float s, e;
@@ -52,13 +62,13 @@ k_dw_reduce(const float *__restrict__ part, int nchunk, int H, float *__restrict
     float a = sh_h[lane][warp], b = sh_l[lane][warp];
     pair_reduce_lanes(a, b, 32);
     const int out = blockIdx.x * 32 + warp;
-    if (lane == 0 && out < H) dw[out] = __fadd_rn(a, b);
+    if (lane == 0 && out < H) st_f32(dw + out, __fadd_rn(a, b));
 }
 
-static cudaError_t launch_dw_reduce(const float *part, int nchunk, int H, float *dw, cudaStream_t s)
+static cudaError_t launch_dw_reduce(const BwdParams &p, int nchunk, float *dw, cudaStream_t s)
 {
-    return launch_pdl(k_dw_reduce, dim3((unsigned)((H + 31) / 32)), dim3(32 * kReduceWarps), 0, s,
-                      part, nchunk, H, dw);
+    return launch_pdl(k_dw_reduce, dim3((unsigned)((p.H + 31) / 32)), dim3(32 * kReduceWarps), 0, s,
+                      (const float *)p.part, nchunk, p.H, dw DW_REDUCE_DEBUG_ARG);
 }
 
 cudaError_t launch_bwd(BwdParams p, bool w32, bool gres, const Layout &L, int sms, float *dw,
@@ -70,7 +80,7 @@ cudaError_t launch_bwd(BwdParams p, bool w32, bool gres, const Layout &L, int sm
                         : (gres ? launch_bwd_bf16w_gres(p, L, sms, &nchunk, s)
                                 : launch_bwd_bf16w_plain(p, L, sms, &nchunk, s));
     if (e != cudaSuccess || p.ncols > 0) return e;
-    return launch_dw_reduce(p.part, nchunk, p.H, dw, s);
+    return launch_dw_reduce(p, nchunk, dw, s);
 }
 
 }  // namespace crmsn

@@ -13,6 +13,69 @@
 
 namespace crmsn {
 
+// ------------------------------------------------------ debug bounds guard --
+// A build with -DCRMSN_DEBUG checks every global load and store of the
+// kernels against the byte ranges of the call's tensors (all of them
+// readable; outputs and the workspace writable) and every access to dynamic
+// shared memory against the size the launch gave.  An access outside them is
+// skipped (a load gives zeros) and the first one is recorded in a device word
+// that crmsn_debug_status() reads back; nothing traps.  In the normal build
+// every check is the constant true and the range table is not passed.
+constexpr int kDebugMaxRanges = 12;
+struct DebugRanges {
+    unsigned long long *word;                    // first violation (0: none)
+    unsigned long long lo[kDebugMaxRanges], hi[kDebugMaxRanges];
+    unsigned writable;                           // bit i: range i may be written
+    int n;
+};
+
+#ifdef CRMSN_DEBUG
+// Kinds of access in a violation word: bits 62..56 kind, 55..32 the CTA,
+// 31..22 the thread, 21..0 the low bits of the global address (of the byte
+// offset for shared memory); bit 63 set.
+enum : unsigned { DBG_LOAD = 1, DBG_STORE = 2, DBG_ASYNC_COPY = 3, DBG_SMEM = 4 };
+static __shared__ DebugRanges dbg_ranges;
+extern __shared__ __align__(16) unsigned char dbg_dyn_smem[];
+
+// Every kernel's first step: the call's ranges into shared memory.
+__device__ __forceinline__ void dbg_enter(const DebugRanges &r)
+{
+    if (threadIdx.x == 0) dbg_ranges = r;
+    __syncthreads();
+}
+static __device__ __noinline__ void dbg_record(unsigned kind, unsigned long long where)
+{
+    const unsigned long long w = (1ull << 63) | ((unsigned long long)kind << 56) |
+                                 ((unsigned long long)(blockIdx.x & 0xffffffu) << 32) |
+                                 ((unsigned long long)(threadIdx.x & 0x3ffu) << 22) |
+                                 (where & 0x3fffffull);
+    if (dbg_ranges.word) atomicCAS(dbg_ranges.word, 0ull, w);
+}
+__device__ __forceinline__ bool dbg_global(const void *p, int bytes, bool write, unsigned kind = 0)
+{
+    const unsigned long long a = (unsigned long long)p, e = a + (unsigned long long)bytes;
+    for (int i = 0; i < dbg_ranges.n; ++i)
+        if (a >= dbg_ranges.lo[i] && e <= dbg_ranges.hi[i] && (!write || ((dbg_ranges.writable >> i) & 1u)))
+            return true;
+    dbg_record(kind ? kind : (write ? DBG_STORE : DBG_LOAD), a);
+    return false;
+}
+__device__ __forceinline__ bool dbg_shared(const void *p, int bytes)
+{
+    unsigned size;
+    asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(size));
+    const long long off = (long long)((const unsigned char *)p - dbg_dyn_smem);
+    if (off >= 0 && off + bytes <= (long long)size) return true;
+    dbg_record(DBG_SMEM, (unsigned long long)off);
+    return false;
+}
+#define CRMSN_DEBUG_ENTER(r) ::crmsn::dbg_enter(r)
+#else
+__device__ __forceinline__ constexpr bool dbg_global(const void *, int, bool, unsigned = 0) { return true; }
+__device__ __forceinline__ constexpr bool dbg_shared(const void *, int) { return true; }
+#define CRMSN_DEBUG_ENTER(r) ((void)0)
+#endif
+
 // ------------------------------------------------------------ BF16 / FP8 --
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -179,6 +242,10 @@ template <int VEC>
 __device__ __forceinline__ BVec<VEC> ld_stream(const uint16_t *p)
 {
     BVec<VEC> v;
+    if (!dbg_global(p, VEC * 2, false)) {
+        for (int i = 0; i < VEC / 2; ++i) v.w[i] = 0u;
+        return v;
+    }
     if constexpr (VEC == 8)
         asm volatile("ld.global.cs.v4.u32 {%0,%1,%2,%3}, [%4];"
                      : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
@@ -192,6 +259,10 @@ template <int VEC>
 __device__ __forceinline__ BVec<VEC> ld_keep(const uint16_t *p)
 {
     BVec<VEC> v;
+    if (!dbg_global(p, VEC * 2, false)) {
+        for (int i = 0; i < VEC / 2; ++i) v.w[i] = 0u;
+        return v;
+    }
     if constexpr (VEC == 8)
         asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
                      : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
@@ -204,6 +275,7 @@ __device__ __forceinline__ BVec<VEC> ld_keep(const uint16_t *p)
 template <int VEC>
 __device__ __forceinline__ void st_stream(uint16_t *p, const BVec<VEC> &v)
 {
+    if (!dbg_global(p, VEC * 2, true)) return;
     if constexpr (VEC == 8)
         asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
                      :: "l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3])
@@ -217,6 +289,7 @@ template <int VEC>
 __device__ __forceinline__ void st_fp8(uint8_t *p, const uint32_t (&c)[VEC / 2])
 {
     // c[i] holds the FP8 pair of elements 2i, 2i+1 in its low 16 bits.
+    if (!dbg_global(p, VEC, true)) return;
     if constexpr (VEC == 8) {
         uint32_t a = (c[0] & 0xffffu) | (c[1] << 16);
         uint32_t b = (c[2] & 0xffffu) | (c[3] << 16);
@@ -231,6 +304,10 @@ __device__ __forceinline__ void st_fp8(uint8_t *p, const uint32_t (&c)[VEC / 2])
 template <int VEC>
 __device__ __forceinline__ void ld_f32_keep(const float *p, float (&f)[VEC])
 {
+    if (!dbg_global(p, VEC * 4, false)) {
+        for (int i = 0; i < VEC; ++i) f[i] = 0.f;
+        return;
+    }
     if constexpr (VEC == 8) {
         asm volatile("ld.global.nc.v4.f32 {%0,%1,%2,%3}, [%4];"
                      : "=f"(f[0]), "=f"(f[1]), "=f"(f[2]), "=f"(f[3]) : "l"(p));
@@ -239,6 +316,18 @@ __device__ __forceinline__ void ld_f32_keep(const float *p, float (&f)[VEC])
     } else {
         asm volatile("ld.global.nc.v2.f32 {%0,%1}, [%2];" : "=f"(f[0]), "=f"(f[1]) : "l"(p));
     }
+}
+
+// One FP32 value through the read-only path, and one plain FP32 store.
+__device__ __forceinline__ float ld_f32_ro(const float *p)
+{
+    if (!dbg_global(p, 4, false)) return 0.f;
+    return __ldg(p);
+}
+__device__ __forceinline__ void st_f32(float *p, float v)
+{
+    if (!dbg_global(p, 4, true)) return;
+    *p = v;
 }
 
 // ------------------------------------------------- compensated reductions --

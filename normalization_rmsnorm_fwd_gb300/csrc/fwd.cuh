@@ -41,30 +41,30 @@
 
 namespace crmsn {
 
-// SiLU of a pair, v / (1 + exp(-v)), as v * RCP(1 + 2^(-v * log2 e)): the
-// products and the sum packed, the base-2 exponential and the reciprocal
-// from the approximate hardware instructions (ex2.approx, rcp.approx).  The
-// relative error stays near 2^-20 (most of it from rounding v * log2 e, up
-// to |v| * 2^-24) -- far below a BF16 half-ulp.  Extremes: for v > ~88 the
-// exponential flushes to 0 and the result is v; for v < ~-87 it exceeds
-// 2^126, the reciprocal flushes to 0 and the result is -0 (|SiLU(v)| is
-// below 1e-35 there); +-inf and NaN give what v * sigmoid(v) gives.
 // Four (two) FP32 values to / from 16-byte (8-byte) aligned shared memory.
 // Plain loads, which the compiler may schedule early (measured: faster than
 // keeping them in program order with the epilogue's stores).
 __device__ __forceinline__ void ld_smem_f32x4(const float *p, float *f)
 {
+    if (!dbg_shared(p, 16)) { f[0] = f[1] = f[2] = f[3] = 0.f; return; }
     const float4 v = *reinterpret_cast<const float4 *>(p);
     f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
 }
 __device__ __forceinline__ void ld_smem_f32x2(const float *p, float *f)
 {
+    if (!dbg_shared(p, 8)) { f[0] = f[1] = 0.f; return; }
     const float2 v = *reinterpret_cast<const float2 *>(p);
     f[0] = v.x; f[1] = v.y;
 }
 __device__ __forceinline__ void st_smem_f32x4(float *p, const float *f)
 {
+    if (!dbg_shared(p, 16)) return;
     *reinterpret_cast<float4 *>(p) = make_float4(f[0], f[1], f[2], f[3]);
+}
+__device__ __forceinline__ void st_smem_f32x2(float *p, float a, float b)
+{
+    if (!dbg_shared(p, 8)) return;
+    *reinterpret_cast<float2 *>(p) = make_float2(a, b);
 }
 
 __device__ __forceinline__ float ex2_approx(float x)
@@ -81,6 +81,14 @@ __device__ __forceinline__ float rcp_approx(float x)
     return y;
 }
 
+// SiLU of a pair, v / (1 + exp(-v)), as v * RCP(1 + 2^(-v * log2 e)): the
+// products and the sum packed, the base-2 exponential and the reciprocal
+// from the approximate hardware instructions (ex2.approx, rcp.approx).  The
+// relative error stays near 2^-20 (most of it from rounding v * log2 e, up
+// to |v| * 2^-24) -- far below a BF16 half-ulp.  Extremes: for v > ~88 the
+// exponential flushes to 0 and the result is v; for v < ~-87 it exceeds
+// 2^126, the reciprocal flushes to 0 and the result is -0 (|SiLU(v)| is
+// below 1e-35 there); +-inf and NaN give what v * sigmoid(v) gives.
 __device__ __forceinline__ F2 silu_f2(F2 v)
 {
     const F2 t = f2_mul(v, f2(-1.4426950408889634f));      // -v * log2(e)
@@ -115,6 +123,7 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
     // (it waits for this whole grid the same way).
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    CRMSN_DEBUG_ENTER(p.dbg);
 
     const int tpr = p.tpr;
     const int grp = row_group(tpr, p.rpc);
@@ -221,9 +230,9 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
     // the exact quotient only next to a rounding midpoint.
     float inv_scale = 1.f;
     if constexpr (OUT == OUT_Q || OUT == OUT_ADA_Q)
-        inv_scale = __frcp_rn(__ldg(p.scale));
+        inv_scale = __frcp_rn(ld_f32_ro(p.scale));
     if constexpr (OUT == OUT_SILU_Q)
-        inv_scale = p.scale != nullptr ? __frcp_rn(__ldg(p.scale)) : 1.f;
+        inv_scale = p.scale != nullptr ? __frcp_rn(ld_f32_ro(p.scale)) : 1.f;
     // The static-scale RMSNorm form scales rstd instead of every value.
     constexpr bool FOLD_SCALE = OUT == OUT_Q && !LN;
 
@@ -354,14 +363,14 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
             reunpack();
             ssum = row_sum(dev_part(t, h, mean), red_h[0]);
             if (p.mean != nullptr && live && lane == 0)
-                p.mean[t] = mean;
+                st_f32(p.mean + t, mean);
         } else {
             ssum = reduced ? part : row_sum(part, red_h[par]);
         }
         reunpack();
         const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ssum, (float)p.H), p.eps)));
         if (p.rstd != nullptr && live && lane == 0)
-            p.rstd[t] = rstd;
+            st_f32(p.rstd + t, rstd);
 
         // ---------------- phase 4: epilogue -----------------------------------
         // o = (h * w) * rstd with h * w exact (WK_MIX), or (h * rstd) * w_eff;
@@ -459,7 +468,7 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
                 if (ok) {
                     st_fp8<VEC>(p.q + t * p.ldq + c, cq);
                     if ((v & 15) == 0)
-                        p.bscale[(int64_t)(v >> 4) * p.ldT + t] = s;
+                        st_f32(p.bscale + (int64_t)(v >> 4) * p.ldT + t, s);
                 }
             } else if constexpr (OUT == OUT_SILU) {
                 BVec<VEC> yv;
@@ -543,8 +552,8 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
                     st_smem_f32x4(ln_gb + p.H + v * 4, b);
                     st_smem_f32x4(ln_gb + p.H + hp + v * 4, b + 4);
                 } else {
-                    *reinterpret_cast<float2 *>(ln_gb + v * 2) = make_float2(g[0], g[1]);
-                    *reinterpret_cast<float2 *>(ln_gb + p.H + v * 2) = make_float2(b[0], b[1]);
+                    st_smem_f32x2(ln_gb + v * 2, g[0], g[1]);
+                    st_smem_f32x2(ln_gb + p.H + v * 2, b[0], b[1]);
                 }
             }
             __syncthreads();
@@ -572,8 +581,8 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
                     st_smem_f32x4(ln_gb + p.H + v * 4, f);
                     st_smem_f32x4(ln_gb + p.H + hp + v * 4, f + 4);
                 } else {
-                    *reinterpret_cast<float2 *>(ln_gb + v * 2) = make_float2(g[0], g[1]);
-                    *reinterpret_cast<float2 *>(ln_gb + p.H + v * 2) = make_float2(f[0], f[1]);
+                    st_smem_f32x2(ln_gb + v * 2, g[0], g[1]);
+                    st_smem_f32x2(ln_gb + p.H + v * 2, f[0], f[1]);
                 }
             }
 #pragma unroll

@@ -66,6 +66,9 @@ struct FwdParams {
     const float *beta;                    // LayerNorm shift [H] (w is gamma)
     float *mean;                          // LayerNorm row means (nullable)
     int tpr;             int rpc;
+#ifdef CRMSN_DEBUG
+    DebugRanges dbg;                      // the call's tensors (debug build)
+#endif
 };
 
 struct BwdParams {
@@ -80,6 +83,9 @@ struct BwdParams {
     int64_t T;           int H;
     int nchunk;          int tpr;         int rpc;
     int ncols;           int colw;        // column form: strips and their width (0: off)
+#ifdef CRMSN_DEBUG
+    DebugRanges dbg;                      // the call's tensors (debug build)
+#endif
 };
 
 // Column form of the backward's dw (bwd.cuh): used when T is at most
