@@ -68,6 +68,38 @@ def test_persistent_forward_rows_do_not_depend_on_T():
         assert torch.equal(y, big_y[:T]) and torch.equal(r, big_r[:T]), T
 
 
+@pytest.mark.parametrize("H,route", [(4096, "bf16"), (5120, "f32"), (1024, "bf16_gres"), (128, "bf16")])
+def test_backward_dx_rows_do_not_depend_on_T(H, route):
+    # A row's dx must not depend on how many rows the call has: neither on
+    # the chunk table nor on the form (up to 2048 rows strip CTAs reduce dw
+    # beside the chunks; above, the chunks write partial rows).  dw differs
+    # only by the rows added, and matches the sum of the parts closely.
+    T = 3000
+    g, x, gr = synth.random_rows(31 + H, T, H, n=3)
+    f32 = route == "f32"
+    w = synth.random_weight(32, H, f32=f32)
+    wd = gu.dev_f32(w) if f32 else gu.dev_bf16(w)
+    gd, xd = gu.dev_bf16(g), gu.dev_bf16(x)
+    grd = gu.dev_bf16(gr) if route == "bf16_gres" else None
+    rstd = gu.dev_f32(np.abs(synth.Draw(33).f32((T,), 0.1, 1.0)))
+    bias = 1.0 if f32 else 0.0
+    big_dx, _ = crm.rmsnorm_bwd(gd, xd, wd, rstd, bias, g_residual=grd)
+    torch.cuda.synchronize()
+    for T2 in (1, 7, 2048, 2049, 2999):
+        dx, _ = crm.rmsnorm_bwd(gd[:T2], xd[:T2], wd, rstd[:T2], bias,
+                                g_residual=None if grd is None else grd[:T2])
+        torch.cuda.synchronize()
+        assert torch.equal(dx.view(torch.int16), big_dx[:T2].view(torch.int16)), T2
+    _, dw_a = crm.rmsnorm_bwd(gd[:2048], xd[:2048], wd, rstd[:2048], bias,
+                              g_residual=None if grd is None else grd[:2048])
+    _, dw_b = crm.rmsnorm_bwd(gd[2048:], xd[2048:], wd, rstd[2048:], bias,
+                              g_residual=None if grd is None else grd[2048:])
+    _, dw_all = crm.rmsnorm_bwd(gd, xd, wd, rstd, bias, g_residual=grd)
+    torch.cuda.synchronize()
+    a, b, c = (t.double().cpu().numpy() for t in (dw_a, dw_b, dw_all))
+    assert np.linalg.norm(a + b - c) <= 1e-6 * np.linalg.norm(c)
+
+
 def test_backward_outputs_stay_inside_their_rows():
     T, H, ld = 70, 1000, 1040
     g, x = synth.random_rows(31, T, H, n=2)
@@ -84,13 +116,14 @@ def test_backward_outputs_stay_inside_their_rows():
     assert (dwg[:32] == -7).all() and (dwg[32 + H:] == -7).all()
 
 
-def test_cuda_graph_replay_matches_eager():
-    # The residual forward and the backward (its dx kernel and the reduce,
-    # launched with programmatic dependent launch) captured once in a CUDA
-    # graph and replayed on new inputs copied into the captured buffers: every
-    # replay equals an eager run bit for bit, and the workspace needs no reset
-    # between replays.
-    T, H = 1024, 2048
+@pytest.mark.parametrize("T", [1024, 2500])
+def test_cuda_graph_replay_matches_eager(T):
+    # The residual forward and the backward (one launch in the column form at
+    # 1024 rows; the chunks and the reduce at 2500, launched with programmatic
+    # dependent launch) captured once in a CUDA graph and replayed on new
+    # inputs copied into the captured buffers: every replay equals an eager
+    # run bit for bit, and the workspace needs no reset between replays.
+    H = 2048
     w = gu.dev_bf16(synth.random_weight(40, H))
     ws = crm.rmsnorm_bwd_workspace(T, H, gu.DEV)
     xs = torch.empty((T, H), dtype=torch.bfloat16, device=gu.DEV)
