@@ -114,3 +114,49 @@ def test_random_shapes(orc, seed):
         return b["dw"], b["dw_abs"]
     parts = gu.each_block(T, H, check)
     gu.check_dw(dwh, sum(p[0] for p in parts), sum(p[1] for p in parts), what=f"{what}: dw")
+
+
+# The other operations on random shapes, through the checks of their own test
+# files: 1x128 block quantisation, AdaRMSNorm (per-row or broadcast style),
+# the gated FP8 path, RMSNorm + SiLU and LayerNorm.
+from test_gpu_ada import compare_ada, compare_gated            # noqa: E402
+from test_gpu_quant import compare_block                       # noqa: E402
+from test_gpu_silu_ln import _check_ln, _check_silu            # noqa: E402
+
+N_OTHER = 40
+
+
+@pytest.mark.parametrize("seed", range(N_OTHER))
+def test_random_shapes_other_ops(orc, seed):
+    rng = np.random.default_rng(5000 + seed)
+    op = seed % 5
+    T = int(np.round(2 ** rng.uniform(0, 11.5)))
+    scale = float(10.0 ** rng.uniform(-1.5, 1.5))
+    if op == 0:
+        H = 128 * int(rng.integers(1, 65))
+        x, r = _rows(rng, T, H, scale), _rows(rng, T, H, scale)
+        compare_block(orc, x, r, _rows(rng, 1, H, 0.1, shift=1.0)[0])
+        return
+    D = int(2 * np.round(2 ** rng.uniform(0, 12)))
+    D = max(2, min(D, 8192))
+    if op in (1, 2):
+        x = _rows(rng, T, D, scale)
+        style = _rows(rng, 1 if rng.random() < 0.5 else T, 3 * D, 0.5)
+        w = _rows(rng, 1, D, 0.1, shift=1.0)[0]
+        if op == 1:
+            compare_ada(orc, x, w, style)
+        else:
+            compare_gated(orc, _rows(rng, T, D, scale), x, _rows(rng, T, D, 1.0), w, style)
+    elif op == 3:
+        x = _rows(rng, T, D, scale)
+        if rng.random() < 0.5:
+            compare_w, bias = (0.02 * rng.standard_normal(D)).astype(np.float32), 1.0
+        else:
+            compare_w, bias = _rows(rng, 1, D, 0.1, shift=1.0)[0], 0.0
+        _check_silu(orc, x, compare_w, bias)
+    else:
+        shift = float(rng.choice([0.0, 0.0, 50.0]))
+        x = _rows(rng, T, D, scale, shift=shift)
+        gamma = (1 + 0.1 * rng.standard_normal(D)).astype(np.float32)
+        beta = (0.1 * rng.standard_normal(D)).astype(np.float32)
+        _check_ln(orc, x, gamma, beta)
