@@ -97,8 +97,9 @@ __device__ __forceinline__ F2 silu_f2(F2 v)
 }
 
 // How the persistent form fetches the next row ahead: 1 = prefetched into
-// L2, 2 = loaded into registers (measured per epilogue).
-constexpr int fwd_prefetch(int in, int out) { return in == IN_LAYERNORM || out == OUT_Q ? 2 : 1; }
+// L2, 2 = loaded into registers (measured per epilogue: the broadcast Ada
+// form 9.7 against 10.2 us with 2; the y form 51.6 against 55.7 us with 1).
+constexpr int fwd_prefetch(int in, int out) { return in == IN_LAYERNORM || out == OUT_Q || out == OUT_ADA ? 2 : 1; }
 
 // The kernel body.  WK is the weight kind (WK_MIX: BF16 weight, no bias,
 // kept packed and multiplied by h exactly with the mixed-precision FMA;
@@ -641,8 +642,8 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
         // slots), starts the loads of row k + 2, then writes row k's outputs
         // -- so the reduction's dependent chain overlaps the next row's
         // arithmetic instead of stalling the CTA.  Measured at T = H = 8192:
-        // 34.5 against 38.7 us; the y and AdaRMSNorm forms, whose L2-only
-        // prefetch keeps them at about 60 registers, lost 9-25 % with it,
+        // 34.5 against 38.7 us; the y and AdaRMSNorm forms, which hold at
+        // most the next row, lost 9-25 % with it,
         // and LayerNorm (three rows in flight, one barrier instead of two per
         // row) lost 19 % at T = 16384, H = 4096.
         constexpr bool PIPED = OUT == OUT_Q && !LN && !SUB;
