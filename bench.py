@@ -555,24 +555,32 @@ def run_e2e(args, world, dev, x, r, g, w, y, rs0, dw, ws):
         e2e_step(step)
     torch.cuda.synchronize()
     ne = max(4, min(args.steps, 20))
-    a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    a_ev.record(s_in[0])
-    for st in s_in[1:] + s_out + [s_cmp]:
-        st.wait_stream(s_in[0])
-    for step in range(ne):
-        e2e_step(step)
-    for st in s_in + s_out[1:] + [s_cmp]:
-        s_out[0].wait_stream(st)
-    b_ev.record(s_out[0])
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(a_ev.elapsed_time(b_ev) / ne, world, dev)
+
+    def timed_pass():
+        a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        a_ev.record(s_in[0])
+        for st in s_in[1:] + s_out + [s_cmp]:
+            st.wait_stream(s_in[0])
+        for step in range(ne):
+            e2e_step(step)
+        for st in s_in + s_out[1:] + [s_cmp]:
+            s_out[0].wait_stream(st)
+        b_ev.record(s_out[0])
+        torch.cuda.synchronize()
+        return max_over_ranks(a_ev.elapsed_time(b_ev) / ne, world, dev)
+
+    # Three passes of ne steps each; the median pass is reported (the host
+    # link is shared with the machine's other work, and one pass can run
+    # into a burst of it).
+    passes = [timed_pass() for _ in range(3)]
+    e2e_ms = sorted(passes)[1]
     best = min(ceiling, key=lambda c: c["both_ms"])
     return {"value": world * STEP_BYTES / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": e2e_ms,
+            "ms_per_step": e2e_ms, "passes_ms_per_step": [round(v, 4) for v in passes],
             "pipelining": f"two buffer sets; {k} copy-in and {k} copy-out streams per direction, "
-                          "one compute stream",
+                          "one compute stream; the median of three passes",
             "copy_ceiling": {"rows": ceiling, "best_both_ms": best["both_ms"],
                              "frac_of_copy_ceiling": round(best["both_ms"] / e2e_ms, 4),
                              "note": "pinned host<->device copies of one step's bytes alone, "
