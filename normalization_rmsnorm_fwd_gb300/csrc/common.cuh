@@ -363,21 +363,6 @@ __device__ __forceinline__ void pair_reduce_lanes(float &h, float &l, int width)
     }
 }
 
-// Sum of the per-warp pairs red_h/red_l[w0 .. w0+nwarp) for every thread of
-// a multi-warp group: each aligned block of next_pow2(nwarp) lanes loads the
-// nwarp pairs (zeros beyond) and reduces them with a butterfly, so every warp
-// of the group computes the same bits in log2 steps.
-__device__ __forceinline__ void pair_reduce_warps(float &h, float &l, const float *red_h,
-                                                  const float *red_l, int w0, int nwarp)
-{
-    int width = 1;
-    while (width < nwarp) width <<= 1;
-    const int i = (threadIdx.x & 31) & (width - 1);
-    h = i < nwarp ? red_h[w0 + i] : 0.f;
-    l = i < nwarp ? red_l[w0 + i] : 0.f;
-    pair_reduce_lanes(h, l, width);
-}
-
 // (h, l) += (bh, bl) without renormalisation (cascaded "Sum2"): the TwoSum
 // error of the leading parts joins the trailing parts.  Symmetric in its two
 // operands, so butterfly partners stay bit-identical.
