@@ -226,7 +226,7 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- GPU side --
 
-def other_kernels(dev, peak, only=None):
+def other_kernels(dev, peak, only=None, widths=False):
     """Each hot-path kernel at its own workload, launched back to back over
     rotating input/output sets whose total is at least 2x the L2 size (at
     most 64 sets: the smallest problems stay L2-resident and are reported as
@@ -235,7 +235,10 @@ def other_kernels(dev, peak, only=None):
     and replayed, one pair of CUDA events around the replays on the
     replaying stream (so the host's per-call cost does not hide small
     kernels); the eager loop's time per Python call is kept as us_eager.
-    `only`: a substring; rows whose name does not contain it are skipped."""
+    `only`: a substring; rows whose name does not contain it are skipped.
+    `widths`: also the width sweep (T * H = 2^26 rows of H = 256 .. 16384:
+    fused residual forward, plain forward, backward, fused add + static
+    FP8), rows named "width sweep: ..."."""
     import torch
 
     import normalization_rmsnorm_fwd_gb300 as crm
@@ -438,6 +441,43 @@ def other_kernels(dev, peak, only=None):
         return make
     add("layernorm bf16 T=16384 H=4096", ln(False), 16384 * 4096 * 4 + 4096 * 8)
     add("layernorm_quant e4m3 T=16384 H=4096", ln(True), 16384 * 4096 * 3 + 4096 * 8 + 4)
+
+    if widths:
+        for Hw in (256, 512, 1024, 2048, 4096, 8192, 16384):
+            Tw = (1 << 26) // Hw
+
+            def sw_res(Tw=Tw, Hw=Hw):
+                x, r = randn(Tw, Hw), randn(Tw, Hw)
+                w = randn(Hw, scale=0.1, shift=1.0)
+                y, hn, rs = torch.empty_like(x), torch.empty_like(x), torch.empty(Tw, device=dev)
+                return lambda: crm.rmsnorm_fwd(x, w, 1e-6, residual=r, y=y, rstd=rs, h_new=hn)
+            add(f"width sweep: rmsnorm_fwd fused residual T={Tw} H={Hw}", sw_res,
+                4 * Tw * Hw * 2 + Hw * 2 + Tw * 4)
+
+            def sw_plain(Tw=Tw, Hw=Hw):
+                x, w = randn(Tw, Hw), randn(Hw, scale=0.1, shift=1.0)
+                y, rs = torch.empty_like(x), torch.empty(Tw, device=dev)
+                return lambda: crm.rmsnorm_fwd(x, w, y=y, rstd=rs)
+            add(f"width sweep: rmsnorm_fwd plain T={Tw} H={Hw}", sw_plain,
+                2 * Tw * Hw * 2 + Hw * 2 + Tw * 4)
+
+            def sw_bwd(Tw=Tw, Hw=Hw):
+                g, x = randn(Tw, Hw), randn(Tw, Hw)
+                w = randn(Hw, scale=0.1, shift=1.0)
+                rstd = torch.rand(Tw, device=dev) + 0.5
+                dx, dw = torch.empty_like(x), torch.empty(Hw, device=dev)
+                ws = crm.rmsnorm_bwd_workspace(Tw, Hw, dev)
+                return lambda: crm.rmsnorm_bwd(g, x, w, rstd, dx=dx, dw=dw, workspace=ws)
+            add(f"width sweep: rmsnorm_bwd T={Tw} H={Hw} (dx + dw, two launches)", sw_bwd,
+                3 * Tw * Hw * 2 + Tw * 4 + Hw * 2 + Hw * 4)
+
+            def sw_q(Tw=Tw, Hw=Hw):
+                x, r = randn(Tw, Hw), randn(Tw, Hw)
+                w = randn(Hw, scale=0.1, shift=1.0)
+                q = torch.empty(Tw, Hw, dtype=torch.float8_e4m3fn, device=dev)
+                return lambda: crm.fused_add_rmsnorm_quant(q, x, r, w, sc)
+            add(f"width sweep: fused_add_rmsnorm_quant e4m3 T={Tw} H={Hw}", sw_q,
+                3 * Tw * Hw * 2 + Tw * Hw + Hw * 2 + 4)
     return out
 
 
@@ -758,8 +798,12 @@ def run_kernel_rows(args):
     dev = torch.device("cuda", local_rank)
     _abi.load()
     peak, _ = measured_peaks()
-    rows = other_kernels(dev, peak, only=args.kernel)
-    print(json.dumps({"impl": "ours", "mode": "kernel rows", "filter": args.kernel,
+    if args.sweep:
+        rows = other_kernels(dev, peak, only="width sweep", widths=True)
+    else:
+        rows = other_kernels(dev, peak, only=args.kernel)
+    print(json.dumps({"impl": "ours", "mode": "width sweep" if args.sweep else "kernel rows",
+                      "filter": "width sweep" if args.sweep else args.kernel,
                       "per_kernel": rows}), flush=True)
 
 
@@ -775,12 +819,15 @@ def main():
     ap.add_argument("--kernel", default=None,
                     help="only run the per-kernel rows whose name contains this text "
                          "(no timed step, no e2e, no CPU baseline; for profiling one kernel)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="only the width sweep: forward, backward and static FP8 at T*H = 2^26 for "
+                         "H = 256 .. 16384 (no timed step, no e2e, no CPU baseline)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
-    elif args.kernel is not None:
+    elif args.kernel is not None or args.sweep:
         run_kernel_rows(args)
     else:
         run_ours(args)
