@@ -706,6 +706,17 @@ __global__ void __launch_bounds__(kFwdMaxThreads) k_rmsnorm_fwd(const FwdParams 
     fwd_body<IN, WK, OUT, FP8K, VEC, VPT, SUB, LOOP>(p);
 }
 
+// The same body for the one-row y and static-FP8 forms of the widest rows
+// (512-thread row groups, 32 elements per thread): launch bounds that ask
+// for two CTAs per SM hold it to 64 registers (measured at T = 4096, H =
+// 16384: 81-93 against 91-112 us for the fused residual forward, 73-86
+// against 84-101 us with the FP8 epilogue, for every weight kind).
+template <int IN, int WK, int OUT, int FP8K, int VEC, int VPT, bool SUB, bool LOOP>
+__global__ void __launch_bounds__(512, 2) k_rmsnorm_fwd_wide(const FwdParams p)
+{
+    fwd_body<IN, WK, OUT, FP8K, VEC, VPT, SUB, LOOP>(p);
+}
+
 // Host-side launch of one kernel.  The persistent form runs on at most
 // (resident CTAs per SM) x (SMs) CTAs; the residency for a block size and
 // shared-memory size is computed once and remembered.
@@ -740,6 +751,10 @@ cudaError_t launch_fwd_kernel(const FwdParams &p, size_t smem, cudaStream_t s)
         const int64_t cap = (int64_t)per_sm * sms;
         if (blocks > cap) blocks = cap;
     }
+    if constexpr (!LOOP && !SUB && VPT == 4 && (OUT == OUT_Y || OUT == OUT_Q))
+        if (threads == 512)
+            return launch_pdl(k_rmsnorm_fwd_wide<IN, WK, OUT, FP8K, VEC, VPT, SUB, LOOP>,
+                              dim3((unsigned)blocks), dim3(threads), smem, s, p);
     return launch_pdl(kern, dim3((unsigned)blocks), dim3(threads), smem, s, p);
 }
 
