@@ -706,11 +706,14 @@ __global__ void __launch_bounds__(kFwdMaxThreads) k_rmsnorm_fwd(const FwdParams 
     fwd_body<IN, WK, OUT, FP8K, VEC, VPT, SUB, LOOP>(p);
 }
 
-// The same body for the one-row y and static-FP8 forms of the widest rows
-// (512-thread row groups, 32 elements per thread): launch bounds that ask
-// for two CTAs per SM hold it to 64 registers (measured at T = 4096, H =
-// 16384: 81-93 against 91-112 us for the fused residual forward, 73-86
-// against 84-101 us with the FP8 epilogue, for every weight kind).
+// The same body for the one-row y, static-FP8 and block-FP8 forms of the
+// widest rows (512-thread row groups, 32 elements per thread): launch
+// bounds that ask for two CTAs per SM hold it to 64 registers (measured at
+// T = 4096, H = 16384: 81-93 against 91-112 us for the fused residual
+// forward, 73-86 against 84-101 us with the static FP8 epilogue, for every
+// weight kind; 98 against 126 us with block FP8).  The AdaRMSNorm, SiLU
+// and LayerNorm one-row forms gain nothing from it, and the gated FP8 form
+// spills (296 against 206 us).
 template <int IN, int WK, int OUT, int FP8K, int VEC, int VPT, bool SUB, bool LOOP>
 __global__ void __launch_bounds__(512, 2) k_rmsnorm_fwd_wide(const FwdParams p)
 {
@@ -751,7 +754,7 @@ cudaError_t launch_fwd_kernel(const FwdParams &p, size_t smem, cudaStream_t s)
         const int64_t cap = (int64_t)per_sm * sms;
         if (blocks > cap) blocks = cap;
     }
-    if constexpr (!LOOP && !SUB && VPT == 4 && (OUT == OUT_Y || OUT == OUT_Q))
+    if constexpr (!LOOP && !SUB && VPT == 4 && (OUT == OUT_Y || OUT == OUT_Q || OUT == OUT_BLOCK))
         if (threads == 512)
             return launch_pdl(k_rmsnorm_fwd_wide<IN, WK, OUT, FP8K, VEC, VPT, SUB, LOOP>,
                               dim3((unsigned)blocks), dim3(threads), smem, s, p);
