@@ -235,10 +235,14 @@ __device__ void dw_columns(const BwdParams &p, int strip, float2 *scratch)
     }
 }
 
-template <bool W32, bool GRES, int VEC, int VPT, bool SUB, int D>
+// WB: a BF16 weight kept as BF16 in shared memory (the bias added as each
+// vector is read) instead of as the FP32 effective weight: half the bytes,
+// which leaves room for a deeper ring on the widest rows (chosen per launch).
+template <bool W32, bool GRES, int VEC, int VPT, bool SUB, int D, bool WB>
 __global__ void __launch_bounds__(kBwdMaxThreads, 1)
 k_rmsnorm_bwd(const BwdParams p)
 {
+    static_assert(!WB || (!W32 && VEC == 8), "a BF16 weight in shared memory needs 16-byte vectors");
     constexpr int NW = VEC / 2;
     constexpr int NT = GRES ? 3 : 2;
     constexpr int S = D + 1;                  // ring stages
@@ -277,11 +281,13 @@ k_rmsnorm_bwd(const BwdParams p)
     // Shared memory: ring [S][stage], then w_eff [VPT*tpr*VEC] (zero past H),
     // then the row-group combine area [rpc][H][2] (when rpc > 1).  w_eff is stored in two
     // planes of four values per vector (one plane for VEC == 2), so that the
-    // 16-byte loads of a warp touch consecutive addresses.
+    // 16-byte loads of a warp touch consecutive addresses; with WB the BF16
+    // weight instead, one 16-byte vector per column vector.
     const int stage_bytes = bwd_stage_bytes(NT, VPT, VEC, nthr);
     unsigned char *ring = dyn_smem;
     float *wsm = reinterpret_cast<float *>(dyn_smem + (size_t)S * stage_bytes);
-    float *comb = wsm + VPT * tpr * VEC;
+    float *comb = wsm + (WB ? VPT * tpr * VEC / 2 : VPT * tpr * VEC);
+    uint16_t *const wsb = reinterpret_cast<uint16_t *>(wsm);
     const int wplane = VPT * tpr * 4;
 
     // This thread's slot of vector k of a tensor in a stage; the per-thread
@@ -297,6 +303,19 @@ k_rmsnorm_bwd(const BwdParams p)
     };
     auto ld_w = [&](int k, F2 (&we)[NW]) {
         const int v = k * tpr + lane;
+        if constexpr (WB) {
+            if (!dbg_shared(wsb + v * VEC, 16)) {
+                for (int e = 0; e < NW; ++e) we[e] = f2(0.f);
+                return;
+            }
+            const uint4 a = *reinterpret_cast<const uint4 *>(wsb + v * VEC);
+            we[0] = f2_bf16(a.x); we[1] = f2_bf16(a.y); we[2] = f2_bf16(a.z); we[3] = f2_bf16(a.w);
+            if (p.bias != 0.f) {
+#pragma unroll
+                for (int e = 0; e < NW; ++e) we[e] = f2_add(we[e], f2(p.bias));
+            }
+            return;
+        }
         if (VEC == 8 ? !dbg_shared(wsm + v * 4, 16) || !dbg_shared(wsm + wplane + v * 4, 16)
                      : !dbg_shared(wsm + v * VEC, 8)) {
             for (int e = 0; e < NW; ++e) we[e] = f2(0.f);
@@ -371,11 +390,33 @@ k_rmsnorm_bwd(const BwdParams p)
                     else
                         *reinterpret_cast<uint32_t *>(slot(st, ti, k)) = 0u;
                 }
-            if (grp == 0)
+            if (grp == 0) {
+                if constexpr (WB) {
+                    if (dbg_shared(wsb + v * VEC, 16))
+                        *reinterpret_cast<uint4 *>(wsb + v * VEC) = make_uint4(0u, 0u, 0u, 0u);
+                } else {
 #pragma unroll
-                for (int i = 0; i < VEC; ++i) st_smem_f32(w_at(v, i), 0.f);
+                    for (int i = 0; i < VEC; ++i) st_smem_f32(w_at(v, i), 0.f);
+                }
+            }
         } else if (grp == 0) {
-            if constexpr (W32) {
+            if constexpr (WB) {
+                // The BF16 weight as it is; with no bias a -0 is stored as +0,
+                // the value f32(w) + 0 of the FP32 form (the bias, when there
+                // is one, is added at each read, with the same rounding).
+                const BVec<VEC> wb = ld_keep<VEC>(static_cast<const uint16_t *>(p.w) + c);
+                uint32_t q[NW];
+#pragma unroll
+                for (int i = 0; i < NW; ++i) {
+                    q[i] = wb.w[i];
+                    if (p.bias == 0.f) {
+                        if ((q[i] & 0xffffu) == 0x8000u) q[i] &= 0xffff0000u;
+                        if ((q[i] >> 16) == 0x8000u) q[i] &= 0x0000ffffu;
+                    }
+                }
+                if (dbg_shared(wsb + v * VEC, 16))
+                    *reinterpret_cast<uint4 *>(wsb + v * VEC) = make_uint4(q[0], q[1], q[2], q[3]);
+            } else if constexpr (W32) {
                 float f[VEC];
                 ld_f32_keep<VEC>(static_cast<const float *>(p.w) + c, f);
 #pragma unroll
@@ -690,10 +731,11 @@ k_rmsnorm_bwd(const BwdParams p)
 }
 
 // Dynamic shared memory of one CTA for a layout and prefetch depth D.
-inline size_t bwd_smem_bytes(bool gres, int vec, int vpt, int threads, int rpc, int H, int D)
+inline size_t bwd_smem_bytes(bool wb, bool gres, int vec, int vpt, int threads, int rpc, int H, int D)
 {
     return (size_t)(D + 1) * bwd_stage_bytes(gres ? 3 : 2, vpt, vec, threads) +
-           ((size_t)vpt * (threads / rpc) * vec + (rpc > 1 ? (size_t)rpc * H * 2 : 0)) * sizeof(float);
+           (size_t)vpt * (threads / rpc) * vec * (wb ? 2 : 4) +
+           (rpc > 1 ? (size_t)rpc * H * 2 * sizeof(float) : 0);
 }
 
 // The most shared memory a CTA may ask for, and the most the backward's
@@ -707,14 +749,14 @@ constexpr size_t kBwdSmemPerSm = 208 * 1024;
 // shared-memory size, computed once per key and remembered) and its launch
 // with a chunk count of at most per_sm x SMs (and at most one chunk per row
 // group).
-template <bool W32, bool GRES, int VEC, int VPT, bool SUB, int D>
+template <bool W32, bool GRES, int VEC, int VPT, bool SUB, int D, bool WB>
 struct BwdInst {
-    static constexpr auto kern = k_rmsnorm_bwd<W32, GRES, VEC, VPT, SUB, D>;
+    static constexpr auto kern = k_rmsnorm_bwd<W32, GRES, VEC, VPT, SUB, D, WB>;
 
     static cudaError_t occupancy(const BwdParams &p, int *per_sm)
     {
         const int threads = p.tpr * p.rpc;
-        const size_t smem = bwd_smem_bytes(GRES, VEC, VPT, threads, p.rpc, p.H, D);
+        const size_t smem = bwd_smem_bytes(WB, GRES, VEC, VPT, threads, p.rpc, p.H, D);
         static std::atomic<int> opted[kOptInDevices];
         cudaError_t e = opt_in_smem(kern, smem, opted);
         if (e != cudaSuccess) return e;
@@ -743,7 +785,7 @@ struct BwdInst {
     static cudaError_t launch(BwdParams p, int per_sm, int sms, int *nchunk_out, cudaStream_t s)
     {
         const int threads = p.tpr * p.rpc;
-        size_t smem = bwd_smem_bytes(GRES, VEC, VPT, threads, p.rpc, p.H, D);
+        size_t smem = bwd_smem_bytes(WB, GRES, VEC, VPT, threads, p.rpc, p.H, D);
         const size_t col_smem = (size_t)(threads / 32) * p.colw * sizeof(float2);
         if (p.ncols > 0 && col_smem > smem) smem = col_smem;
         const int64_t by_rows = (p.T + p.rpc - 1) / p.rpc;
@@ -759,25 +801,33 @@ struct BwdInst {
 // Calls f(BwdInst<...>{}) for the instantiation of a layout (SUB groups with
 // VPT 1|2; multi-warp groups with VPT 1|2|4 for 16-byte vectors, 1|2|4|8|16
 // for 4-byte vectors; the unpipelined D = 0 form only for 32 elements per
-// thread).
+// thread; the BF16 weight in shared memory (wb) only for a BF16 weight with
+// 32 elements per thread in 16-byte vectors and a ring).
 template <bool W32, bool GRES, int VEC, int D, typename F>
-cudaError_t with_bwd_inst(const Layout &L, F &&f)
+cudaError_t with_bwd_inst(const Layout &L, bool wb, F &&f)
 {
     constexpr int V32 = 32 / VEC;
     if constexpr (D == 0) {
-        if (!L.sub && L.vpt == V32) return f(BwdInst<W32, GRES, VEC, V32, false, 0>{});
+        if (!wb && !L.sub && L.vpt == V32) return f(BwdInst<W32, GRES, VEC, V32, false, 0, false>{});
         return cudaErrorInvalidConfiguration;
     } else {
+        if constexpr (!W32 && VEC == 8) {
+            if (wb) {
+                if (!L.sub && L.vpt == 4) return f(BwdInst<W32, GRES, VEC, 4, false, D, true>{});
+                return cudaErrorInvalidConfiguration;
+            }
+        }
+        if (wb) return cudaErrorInvalidConfiguration;
         if (L.sub) {
-            if (L.vpt == 1) return f(BwdInst<W32, GRES, VEC, 1, true, D>{});
-            if (L.vpt == 2) return f(BwdInst<W32, GRES, VEC, 2, true, D>{});
+            if (L.vpt == 1) return f(BwdInst<W32, GRES, VEC, 1, true, D, false>{});
+            if (L.vpt == 2) return f(BwdInst<W32, GRES, VEC, 2, true, D, false>{});
         } else {
-            if (L.vpt == 1) return f(BwdInst<W32, GRES, VEC, 1, false, D>{});
-            if (L.vpt == 2) return f(BwdInst<W32, GRES, VEC, 2, false, D>{});
-            if (L.vpt == 4) return f(BwdInst<W32, GRES, VEC, 4, false, D>{});
+            if (L.vpt == 1) return f(BwdInst<W32, GRES, VEC, 1, false, D, false>{});
+            if (L.vpt == 2) return f(BwdInst<W32, GRES, VEC, 2, false, D, false>{});
+            if (L.vpt == 4) return f(BwdInst<W32, GRES, VEC, 4, false, D, false>{});
             if constexpr (VEC == 2) {
-                if (L.vpt == 8) return f(BwdInst<W32, GRES, VEC, 8, false, D>{});
-                if (L.vpt == 16) return f(BwdInst<W32, GRES, VEC, 16, false, D>{});
+                if (L.vpt == 8) return f(BwdInst<W32, GRES, VEC, 8, false, D, false>{});
+                if (L.vpt == 16) return f(BwdInst<W32, GRES, VEC, 16, false, D, false>{});
             }
         }
         return cudaErrorInvalidConfiguration;
@@ -785,13 +835,13 @@ cudaError_t with_bwd_inst(const Layout &L, F &&f)
 }
 
 template <bool W32, bool GRES, int VEC, typename F>
-cudaError_t with_bwd_depth(int D, const Layout &L, F &&f)
+cudaError_t with_bwd_depth(int D, const Layout &L, bool wb, F &&f)
 {
     switch (D) {
-        case 3: return with_bwd_inst<W32, GRES, VEC, 3>(L, f);
-        case 2: return with_bwd_inst<W32, GRES, VEC, 2>(L, f);
-        case 1: return with_bwd_inst<W32, GRES, VEC, 1>(L, f);
-        default: return with_bwd_inst<W32, GRES, VEC, 0>(L, f);
+        case 3: return with_bwd_inst<W32, GRES, VEC, 3>(L, wb, f);
+        case 2: return with_bwd_inst<W32, GRES, VEC, 2>(L, wb, f);
+        case 1: return with_bwd_inst<W32, GRES, VEC, 1>(L, wb, f);
+        default: return with_bwd_inst<W32, GRES, VEC, 0>(L, wb, f);
     }
 }
 
@@ -799,42 +849,67 @@ cudaError_t with_bwd_depth(int D, const Layout &L, F &&f)
 // shared memory, the one with the most rows in flight per SM (CTAs per SM --
 // capped at bwd_max_ctas_per_sm(H) and at what kBwdSmemPerSm holds --
 // times the depth), the larger CTA count on a tie; D = 0 (no ring) only
-// when no ring fits.
+// when no ring fits.  The pipelined loop overlaps the loads with the
+// arithmetic only from D = 2 on (it waits for row i + 1 while row i + D is
+// issued); where the FP32 weight leaves it at D <= 1 (a BF16 weight, 32
+// elements per thread: H above about 14500, or with g_residual above about
+// 10500) the weight is held as BF16 if that gives a deeper ring (measured
+// at T = H = 16384: 310 -> 271 us, with g_residual 459 -> 363 us; where
+// the depth is the same it costs about 5 %, the conversion at each read).
 template <bool W32, bool GRES, int VEC>
 cudaError_t launch_bwd_vec(const BwdParams &p, const Layout &L, int sms, int *nc, cudaStream_t s)
 {
     const int threads = p.tpr * p.rpc;
     const int cap = bwd_max_ctas_per_sm(p.H);
-    int best_d = 0, best_n = 1;
-    long best_score = -1;
-    for (int d = 3; d >= 1; --d) {
-        const size_t smem = bwd_smem_bytes(GRES, VEC, L.vpt, threads, p.rpc, p.H, d);
-        if (smem > kBwdSmemMax) continue;
-        int n = 0;
-        cudaError_t e = with_bwd_depth<W32, GRES, VEC>(d, L, [&](auto inst) {
-            return decltype(inst)::occupancy(p, &n);
-        });
+    auto choose = [&](bool wb, int &best_d, int &best_n) -> cudaError_t {
+        best_d = -1;
+        best_n = 1;
+        long best_score = -1;
+        for (int d = 3; d >= 1; --d) {
+            const size_t smem = bwd_smem_bytes(wb, GRES, VEC, L.vpt, threads, p.rpc, p.H, d);
+            if (smem > kBwdSmemMax) continue;
+            int n = 0;
+            cudaError_t e = with_bwd_depth<W32, GRES, VEC>(d, L, wb, [&](auto inst) {
+                return decltype(inst)::occupancy(p, &n);
+            });
+            if (e != cudaSuccess) return e;
+            if (n > cap) n = cap;
+            const int by_budget = (int)(kBwdSmemPerSm / (smem + 1024));
+            if (n > by_budget) n = by_budget > 0 ? by_budget : 1;
+            if (n < 1) continue;
+            const long score = (long)n * d * 16 + n;
+            if (score > best_score) {
+                best_score = score;
+                best_d = d;
+                best_n = n;
+            }
+        }
+        return cudaSuccess;
+    };
+    int best_d = -1, best_n = 1;
+    bool wb = false;
+    cudaError_t e = choose(false, best_d, best_n);
+    if (e != cudaSuccess) return e;
+    if (!W32 && VEC == 8 && !L.sub && L.vpt == 4 && best_d <= 1) {
+        int d2 = -1, n2 = 1;
+        e = choose(true, d2, n2);
         if (e != cudaSuccess) return e;
-        if (n > cap) n = cap;
-        const int by_budget = (int)(kBwdSmemPerSm / (smem + 1024));
-        if (n > by_budget) n = by_budget > 0 ? by_budget : 1;
-        if (n < 1) continue;
-        const long score = (long)n * d * 16 + n;
-        if (score > best_score) {
-            best_score = score;
-            best_d = d;
-            best_n = n;
+        if (d2 > best_d) {
+            wb = true;
+            best_d = d2;
+            best_n = n2;
         }
     }
-    if (best_score < 0) {
-        cudaError_t e = with_bwd_depth<W32, GRES, VEC>(0, L, [&](auto inst) {
+    if (best_d < 0) {
+        best_d = 0;
+        e = with_bwd_depth<W32, GRES, VEC>(0, L, false, [&](auto inst) {
             return decltype(inst)::occupancy(p, &best_n);
         });
         if (e != cudaSuccess) return e;
         if (best_n < 1) return cudaErrorInvalidConfiguration;
         if (best_n > cap) best_n = cap;
     }
-    return with_bwd_depth<W32, GRES, VEC>(best_d, L, [&](auto inst) {
+    return with_bwd_depth<W32, GRES, VEC>(best_d, L, wb, [&](auto inst) {
         return decltype(inst)::launch(p, best_n, sms, nc, s);
     });
 }

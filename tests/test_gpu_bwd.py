@@ -64,7 +64,9 @@ def test_plain_small_config(orc):
 
 
 # 8192 with g_residual, 9002 with g_residual (4-byte path) and 12288 run the
-# backward with two rows in flight (three ring stages fit, four do not).
+# backward with two rows in flight (three ring stages fit, four do not);
+# 16384 holds the BF16 weight as BF16 in shared memory (two rows in flight,
+# one with g_residual; the FP32 weight: one, or with g_residual no ring).
 # 300 rows take dw from the column CTAs, 2500 rows from the chunks' partial
 # rows and the reduction kernel.
 @pytest.mark.parametrize("H", [2, 8, 64, 128, 200, 256, 520, 1024, 2048, 3072, 4096, 5120,
@@ -193,3 +195,26 @@ def test_pipelined_chunk_lengths(orc, H, T):
     w = synth.random_weight(T + 7, H)
     compare(orc, g, x, w)
 
+
+
+@pytest.mark.parametrize("H,gres", [(16384, False), (11264, True)])
+@pytest.mark.parametrize("bias", [0.0, 1.0])
+@pytest.mark.parametrize("T", [300, 2500])
+def test_bf16_weight_held_as_bf16_matches_fp32_weight(orc, H, gres, bias, T):
+    # At these widths a BF16 weight is held as BF16 in shared memory (which
+    # leaves room for a deeper ring than the FP32 weight does); the same
+    # weight values given as FP32 take the FP32 table and a shallower ring.
+    # Both run the same pipelined arithmetic, so dx and dw agree bit for bit;
+    # a few weights are -0 (with no bias the FP32 table holds +0 there).
+    g, x, gr = synth.random_rows(H + T + 5, T, H, n=3)
+    w = synth.random_weight(H + 6, H)
+    w[::997] = 0x8000
+    w32 = (w.astype(np.uint32) << 16).view(np.float32)       # the same values, exactly
+    rstd = np.abs(synth.Draw(H + 7).f32((T,), 0.1, 1.0))
+    g_res = gr if gres else None
+    dx_b, dw_b = run_bwd(g, x, w, rstd, bias, g_res)
+    dx_f, dw_f = run_bwd(g, x, w32, rstd, bias, g_res)
+    assert np.array_equal(dx_b, dx_f)
+    assert np.array_equal(dw_b.view(np.uint32), dw_f.view(np.uint32))
+    if T == 300:
+        check_every_row(orc, g, x, w, rstd, dx_b, dw_b, bias, g_res)

@@ -188,11 +188,12 @@ def test_layernorm(dbg, monkeypatch, T, H, fp8):
 
 
 @pytest.mark.parametrize("T,H", [(1, 4096), (37, 128), (37, 1022), (300, 4096), (300, 5120),
-                                 (2500, 4096), (2500, 128), (2049, 1024), (40, 16384)])
+                                 (2500, 4096), (2500, 128), (2049, 1024), (40, 16384), (2100, 11264)])
 @pytest.mark.parametrize("route", ["bf16", "f32", "bf16_gres"])
 def test_backward(dbg, monkeypatch, T, H, route):
     # Up to 2048 rows the column form (strip CTAs beside the chunks), above
-    # it the chunk table, its partial rows and the reduction kernel.
+    # it the chunk table, its partial rows and the reduction kernel; at
+    # H = 16384 (and 11264 with g_residual) a BF16 weight is held as BF16.
     def case():
         g = _gen(17 * T + H)
         gr = _rows(g, T, H)
