@@ -98,8 +98,14 @@ __device__ __forceinline__ F2 silu_f2(F2 v)
 
 // How the persistent form fetches the next row ahead: 1 = prefetched into
 // L2, 2 = loaded into registers (measured per epilogue: the broadcast Ada
-// form 9.7 against 10.2 us with 2; the y form 51.6 against 55.7 us with 1).
-constexpr int fwd_prefetch(int in, int out) { return in == IN_LAYERNORM || out == OUT_Q || out == OUT_ADA ? 2 : 1; }
+// form 9.7 against 10.2 us with 2; the y form 51.6 against 55.7 us with 1;
+// LayerNorm with 64 elements per thread, BF16 out, T = 16384, H = 4096:
+// 46.5 against 53.0 us with 1).
+constexpr int fwd_prefetch(int in, int out, int vpt)
+{
+    if (in == IN_LAYERNORM) return vpt <= 4 ? 2 : 1;
+    return out == OUT_Q || out == OUT_ADA ? 2 : 1;
+}
 
 // The kernel body.  WK is the weight kind (WK_MIX: BF16 weight, no bias,
 // kept packed and multiplied by h exactly with the mixed-precision FMA;
@@ -551,7 +557,7 @@ __device__ __forceinline__ void fwd_body(const FwdParams &p)
         load_weights();
         const int64_t stride = (int64_t)gridDim.x * p.rpc;
         const int64_t b0 = (int64_t)blockIdx.x * p.rpc;
-        constexpr int PF = fwd_prefetch(IN, OUT);
+        constexpr int PF = fwd_prefetch(IN, OUT, VPT);
         load_row(b0 + grp, xa, false);
         if constexpr (LN_SMEM) {
             // gamma and beta into shared memory, the whole CTA striding over
@@ -804,7 +810,8 @@ cudaError_t launch_fwd_inst(const FwdParams &p, cudaStream_t s)
 
 // Dispatch over the row layouts the host chooser can return: SUB groups with
 // VPT 1|2; multi-warp groups with VPT 2|4 (16-byte vectors) or 2|4|8|16
-// (4-byte vectors), i.e. at most 32 elements per thread.
+// (4-byte vectors), i.e. at most 32 elements per thread; and LayerNorm with
+// BF16 output also VPT 8 of 16-byte vectors (64 elements per thread).
 template <int IN, int WK, int OUT, int FP8K, int VEC>
 cudaError_t launch_fwd_vec(const FwdParams &p, int vpt, bool sub, cudaStream_t s)
 {
@@ -814,6 +821,8 @@ cudaError_t launch_fwd_vec(const FwdParams &p, int vpt, bool sub, cudaStream_t s
     } else {
         if (vpt == 2) return launch_fwd_inst<IN, WK, OUT, FP8K, VEC, 2, false>(p, s);
         if (vpt == 4) return launch_fwd_inst<IN, WK, OUT, FP8K, VEC, 4, false>(p, s);
+        if constexpr (VEC == 8 && IN == IN_LAYERNORM && OUT == OUT_Y)
+            if (vpt == 8) return launch_fwd_inst<IN, WK, OUT, FP8K, VEC, 8, false>(p, s);
         if constexpr (VEC == 2) {
             if (vpt == 8) return launch_fwd_inst<IN, WK, OUT, FP8K, VEC, 8, false>(p, s);
             if (vpt == 16) return launch_fwd_inst<IN, WK, OUT, FP8K, VEC, 16, false>(p, s);

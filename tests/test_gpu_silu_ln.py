@@ -223,3 +223,28 @@ def test_layernorm_strided_in_place(orc):
     ref = orc.layernorm(xs, g, b, 1e-5)
     allow = _ln_allowance(orc.bf16_to_f64(xs), ref, g, b)
     gu.check_bf16(gu.host_bits(xd), ref["v_exact"], allowance=allow, what="layernorm in place")
+
+
+@pytest.mark.parametrize("H", [4096, 8192])
+def test_layernorm_bf16_64_elements_per_thread(orc, H):
+    # BF16 LayerNorm at H = 4096 and 8192 runs 64 elements per thread (two or
+    # four warps a row, several rows per group, the next row prefetched into
+    # L2 only): every row against the oracle, with rows of a large common
+    # offset and a constant row; then the same rows at a row stride of 2H with
+    # the output in place, bit for bit equal to the contiguous call.
+    T = 1500
+    gen = torch.Generator().manual_seed(H)
+    v = torch.randn(T, H, generator=gen)
+    v[::3] += 300.0
+    v[7] = 2.5
+    x = synth.bf16_bits(v)
+    g, b = _gamma_beta(H + 9, H)
+    _check_ln(orc, x, g, b, kinds=())
+    gd, bd = gu.dev_f32(g), gu.dev_f32(b)
+    y = crm.layernorm(gu.dev_bf16(x), gd, bd, 1e-5)
+    buf = np.zeros((T, 2 * H), np.uint16)
+    buf[:, H:] = x
+    xs = gu.dev_bf16(buf)[:, H:]
+    crm.layernorm(xs, gd, bd, 1e-5, out=xs)
+    torch.cuda.synchronize()
+    assert np.array_equal(gu.host_bits(xs), gu.host_bits(y))
