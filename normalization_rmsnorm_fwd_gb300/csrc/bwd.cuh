@@ -401,15 +401,17 @@ k_rmsnorm_bwd(const BwdParams p)
             }
         } else if (grp == 0) {
             if constexpr (WB) {
-                // The BF16 weight as it is; with no bias a -0 is stored as +0,
-                // the value f32(w) + 0 of the FP32 form (the bias, when there
-                // is one, is added at each read, with the same rounding).
+                // The BF16 weight as it is; with a bias of +0 a -0 is stored as
+                // +0, the value f32(w) + 0 of the FP32 form (a nonzero bias is
+                // added at each read, with the same rounding; adding -0
+                // changes nothing).
                 const BVec<VEC> wb = ld_keep<VEC>(static_cast<const uint16_t *>(p.w) + c);
+                const bool plus_zero = __float_as_uint(p.bias) == 0u;
                 uint32_t q[NW];
 #pragma unroll
                 for (int i = 0; i < NW; ++i) {
                     q[i] = wb.w[i];
-                    if (p.bias == 0.f) {
+                    if (plus_zero) {
                         if ((q[i] & 0xffffu) == 0x8000u) q[i] &= 0xffff0000u;
                         if ((q[i] >> 16) == 0x8000u) q[i] &= 0x0000ffffu;
                     }

@@ -198,14 +198,15 @@ def test_pipelined_chunk_lengths(orc, H, T):
 
 
 @pytest.mark.parametrize("H,gres", [(16384, False), (11264, True)])
-@pytest.mark.parametrize("bias", [0.0, 1.0])
+@pytest.mark.parametrize("bias", [0.0, -0.0, 1.0])
 @pytest.mark.parametrize("T", [300, 2500])
 def test_bf16_weight_held_as_bf16_matches_fp32_weight(orc, H, gres, bias, T):
     # At these widths a BF16 weight is held as BF16 in shared memory (which
     # leaves room for a deeper ring than the FP32 weight does); the same
     # weight values given as FP32 take the FP32 table and a shallower ring.
     # Both run the same pipelined arithmetic, so dx and dw agree bit for bit;
-    # a few weights are -0 (with no bias the FP32 table holds +0 there).
+    # a few weights are -0 (with a bias of +0 the FP32 table holds +0 there,
+    # with a bias of -0 it keeps -0).
     g, x, gr = synth.random_rows(H + T + 5, T, H, n=3)
     w = synth.random_weight(H + 6, H)
     w[::997] = 0x8000
